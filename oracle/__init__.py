@@ -1,0 +1,22 @@
+"""CPU float64 oracle for exact attention.  TEST INFRASTRUCTURE ONLY.
+
+Imported by ``tests/``, ``__graft_entry__.smoke()`` and the bench's CPU
+baseline / reference arm, and by nothing else.  Parity: pinned (see
+``tests/test_oracle_pins.py``); every function here has at least one pin that
+does not re-use its own formula.
+"""
+from .attention import (  # noqa: F401
+    LN2,
+    backward,
+    flops_backward,
+    flops_forward,
+    forward,
+    forward_fp8_reference,
+    head_backward,
+    head_forward,
+    head_forward_online,
+    online_softmax_vector,
+    row_dot,
+    scores,
+    softmax_stats,
+)

@@ -1,0 +1,311 @@
+"""Pins for the float64 oracle: each check comes from something other than the
+oracle's own formula -- closed forms, invariants, the pages' identities, brute
+force on tiny inputs, finite differences, or a library routine.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_76_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+def rand_qkv(n, d, seed, n_k=None):
+    r = rng(seed)
+    n_k = n if n_k is None else n_k
+    return r.standard_normal((n, d)), r.standard_normal((n_k, d)), r.standard_normal((n_k, d))
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_query_gives_mean_of_values(causal):
+    # Q = 0 makes every score 0: P is uniform over the unmasked keys.
+    n, d = 37, 5
+    _, k, v = rand_qkv(n, d, 1)
+    q = np.zeros((n, d))
+    o, lse, _ = oracle.head_forward(q, k, v, causal, 0.3)
+    for i in range(n):
+        cnt = i + 1 if causal else n
+        np.testing.assert_allclose(o[i], v[:cnt].mean(axis=0), rtol=0, atol=1e-13)
+        assert abs(lse[i] - math.log(cnt)) < 1e-13
+
+
+def test_causal_row_zero_is_first_value():
+    n, d, s = 19, 8, 0.7
+    q, k, v = rand_qkv(n, d, 2)
+    o, lse, _ = oracle.head_forward(q, k, v, True, s)
+    np.testing.assert_array_equal(o[0], v[0])
+    assert abs(lse[0] - s * float(q[0] @ k[0])) < 1e-13
+
+
+def test_dominant_logit_selects_its_value_row():
+    n, d, s = 16, 8, 1.0
+    q, k, v = rand_qkv(n, d, 3)
+    i, jstar, c = 5, 11, 60.0
+    k = k * 0.01
+    k[jstar] = c * q[i] / np.linalg.norm(q[i])
+    o, _, _ = oracle.head_forward(q, k, v, False, s)
+    # every other logit is at most |q_i| * max|k_j| with k_j tiny
+    gap = s * c * np.linalg.norm(q[i]) - s * np.linalg.norm(q[i]) * np.abs(k[np.arange(n) != jstar]).sum(1).max()
+    bound = (n - 1) * math.exp(-gap) * 2 * np.abs(v).max()
+    assert np.abs(o[i] - v[jstar]).max() <= bound + 1e-15
+
+
+def test_two_key_softmax_is_logistic():
+    # With two keys the softmax weight of key 0 is the logistic function of the
+    # score difference: sigma(x) = 1 / (1 + e^-x).
+    q = np.array([[1.5, -0.5]])
+    k = np.array([[0.8, 0.3], [-0.2, 0.9]])
+    v = np.array([[2.0, -1.0], [0.5, 4.0]])
+    s = 0.9
+    x = s * (q[0] @ k[0] - q[0] @ k[1])
+    w0 = 1.0 / (1.0 + math.exp(-x))
+    o, lse, _ = oracle.head_forward(q, k, v, False, s)
+    np.testing.assert_allclose(o[0], w0 * v[0] + (1 - w0) * v[1], rtol=0, atol=1e-15)
+    s0, s1 = s * q[0] @ k[0], s * q[0] @ k[1]
+    assert abs(lse[0] - (max(s0, s1) + math.log1p(math.exp(-abs(s0 - s1))))) < 1e-14
+
+
+# ---------------------------------------------------------------- brute force
+
+def brute_force_head(q, k, v, causal, s):
+    """Scalar loops with math.exp: independent of the vectorised oracle."""
+    n, d = len(q), len(q[0])
+    o, lse = [], []
+    for i in range(n):
+        keys = range(i + 1) if causal else range(len(k))
+        logits = [s * sum(q[i][t] * k[j][t] for t in range(d)) for j in keys]
+        mx = max(logits)
+        w = [math.exp(x - mx) for x in logits]
+        tot = sum(w)
+        o.append([sum(w[a] * v[j][t] for a, j in enumerate(keys)) / tot for t in range(len(v[0]))])
+        lse.append(mx + math.log(tot))
+    return np.array(o), np.array(lse)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_brute_force_tiny(causal):
+    q, k, v = rand_qkv(6, 3, 4)
+    o, lse, _ = oracle.head_forward(q, k, v, causal, 0.45)
+    ob, lb = brute_force_head(q.tolist(), k.tolist(), v.tolist(), causal, 0.45)
+    np.testing.assert_allclose(o, ob, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lb, rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_probability_rows_sum_to_one(causal):
+    q, k, v = rand_qkv(50, 16, 5)
+    _, _, p = oracle.head_forward(q, k, v, causal, 0.25)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    if causal:
+        assert np.all(p[np.triu_indices(50, 1)] == 0.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_shift_of_keys(causal):
+    # K_j <- K_j + c for all j adds s*q_i.c to every logit of row i: O is
+    # unchanged and L_i moves by exactly that amount.
+    n, d, s = 40, 6, 0.4
+    q, k, v = rand_qkv(n, d, 6)
+    c = rng(7).standard_normal(d)
+    o1, l1, _ = oracle.head_forward(q, k, v, causal, s)
+    o2, l2, _ = oracle.head_forward(q, k + c, v, causal, s)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1 + s * (q @ c), rtol=0, atol=1e-12)
+
+
+def test_key_value_permutation_non_causal():
+    q, k, v = rand_qkv(33, 7, 8)
+    perm = rng(9).permutation(33)
+    o1, l1, _ = oracle.head_forward(q, k, v, False, 0.5)
+    o2, l2, _ = oracle.head_forward(q, k[perm], v[perm], False, 0.5)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_orthogonal_rotation_of_q_and_k(causal):
+    # "FLASH-ATTN", Low-precision with FP8 (incoherent processing): for an
+    # orthogonal M, (QM)(KM)^T = QK^T, so the output does not change.
+    n, d = 30, 16
+    q, k, v = rand_qkv(n, d, 10)
+    m, _ = np.linalg.qr(rng(11).standard_normal((d, d)))
+    o1, l1, _ = oracle.head_forward(q, k, v, causal, 0.25)
+    o2, l2, _ = oracle.head_forward(q @ m, k @ m, v, causal, 0.25)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_column_sums(causal):
+    # Rows of dS sum to zero, so sum_j dK_j = 0; rows of P sum to one, so
+    # sum_j dV_j = sum_i dO_i.
+    n, d = 45, 8
+    q, k, v = rand_qkv(n, d, 12)
+    do = rng(13).standard_normal((n, d))
+    dq, dk, dv, dvec = oracle.head_backward(q, k, v, do, causal, 0.35)
+    np.testing.assert_allclose(dk.sum(axis=0), 0.0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv.sum(axis=0), do.sum(axis=0), rtol=0, atol=1e-12)
+    o, _, _ = oracle.head_forward(q, k, v, causal, 0.35)
+    np.testing.assert_allclose(dvec, (do * o).sum(axis=1), rtol=0, atol=1e-12)
+
+
+def test_row_dot_matches_definition():
+    q, k, v = rand_qkv(20, 4, 14)
+    do = rng(15).standard_normal((20, 4))
+    o, _, p = oracle.head_forward(q, k, v, True, 0.5)
+    dp = do @ v.T
+    got = oracle.row_dot(o[None, None], do[None, None])[0, 0]
+    np.testing.assert_allclose(got, (p * dp).sum(1), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- online == two-pass
+
+@pytest.mark.parametrize("block", [1, 7, 64, 200])
+def test_online_softmax_vector(block):
+    x = rng(16).standard_normal(200) * 5
+    y, m, ell = oracle.online_softmax_vector(x, block)
+    e = np.exp(x - x.max())
+    np.testing.assert_allclose(y, e / e.sum(), rtol=0, atol=1e-15)
+    assert m == x.max()
+    assert abs(ell - e.sum()) < 1e-12 * e.sum()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("block", [1, 7, 64, 130])
+@pytest.mark.parametrize("tau", [0.0, 8 * math.log(2.0)])
+def test_online_fa2_equals_definition(causal, block, tau):
+    n, d, s = 130, 16, 0.3
+    q, k, v = rand_qkv(n, d, 17)
+    q *= 3.0  # spread the logits so the running max moves between blocks
+    o1, l1, _ = oracle.head_forward(q, k, v, causal, s)
+    o2, l2 = oracle.head_forward_online(q, k, v, causal, s, block, tau)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- finite differences
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradients_by_central_differences(causal):
+    n, d, s, h = 8, 4, 0.6, 1e-6
+    q, k, v = rand_qkv(n, d, 18)
+    do = rng(19).standard_normal((n, d))
+
+    def loss(qq, kk, vv):
+        o, _, _ = oracle.head_forward(qq, kk, vv, causal, s)
+        return float((o * do).sum())
+
+    dq, dk, dv, _ = oracle.head_backward(q, k, v, do, causal, s)
+    for x, g, idx in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        fd = np.zeros_like(x)
+        for a in range(n):
+            for b in range(d):
+                xp = x.copy(); xp[a, b] += h
+                xm = x.copy(); xm[a, b] -= h
+                args_p = [q, k, v]; args_p[idx] = xp
+                args_m = [q, k, v]; args_m[idx] = xm
+                fd[a, b] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(fd - g).max() / np.abs(g).max()
+        assert err <= 1e-6, (idx, err)
+
+
+def test_gradients_fd_on_tiny_workload_entries():
+    w = inputs.TINY
+    q, k, v, do = (t.double().numpy() for t in inputs.draw_fp32(w.B, w.H, w.N, w.d, w.seed))
+    b, hh = 0, 1
+    qh, kh, vh, doh = q[b, hh], k[b, hh], v[b, hh], do[b, hh]
+    dq, dk, dv, _ = oracle.head_backward(qh, kh, vh, doh, w.causal, w.scale)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        o, _, _ = oracle.head_forward(qq, kk, vv, w.causal, w.scale)
+        return float((o * doh).sum())
+
+    for (idx, g) in ((0, dq), (1, dk), (2, dv)):
+        for (a, c) in ((0, 0), (17, 33), (127, 63)):
+            base = [qh, kh, vh]
+            xp = [t.copy() for t in base]; xp[idx][a, c] += h
+            xm = [t.copy() for t in base]; xm[idx][a, c] -= h
+            fd = (loss(*xp) - loss(*xm)) / (2 * h)
+            assert abs(fd - g[a, c]) <= 1e-6 * max(1.0, np.abs(g).max()), (idx, a, c, fd, g[a, c])
+
+
+# ---------------------------------------------------------------- library routine
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_against_torch_sdpa_float64(causal):
+    w = inputs.GPT2
+    q, k, v, do = inputs.draw_bf16(1, 3, 256, w.d, w.seed)
+    q64, k64, v64, do64 = (t.double().requires_grad_(True) for t in (q, k, v, do))
+    o_t = torch.nn.functional.scaled_dot_product_attention(q64, k64, v64, is_causal=causal, scale=w.scale)
+    o_t.backward(do64)
+    o, lse = oracle.forward(q, k, v, causal, w.scale)
+    np.testing.assert_allclose(o, o_t.detach().numpy(), rtol=0, atol=1e-12)
+    s = w.scale * (q64.detach() @ k64.detach().transpose(-1, -2))
+    if causal:
+        s = s.masked_fill(torch.ones(256, 256, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), rtol=0, atol=1e-12)
+    dq, dk, dv = oracle.backward(q, k, v, do, causal, w.scale)
+    np.testing.assert_allclose(dq, q64.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, k64.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, v64.grad.numpy(), rtol=0, atol=1e-11)
+
+
+def test_sampled_heads_match_full():
+    q, k, v, do = inputs.draw_bf16(2, 3, 64, 16, 5)
+    o_full, l_full = oracle.forward(q, k, v, True, 0.25)
+    o_s, l_s = oracle.forward(q, k, v, True, 0.25, heads=[(1, 2)])
+    np.testing.assert_array_equal(o_s[1, 2], o_full[1, 2])
+    assert np.isnan(o_s[0, 0]).all() and np.isnan(l_s[0, 1]).all()
+
+
+# ---------------------------------------------------------------- page figures
+
+def test_page_figures():
+    items = {i["id"]: i for i in json.load(open(os.path.join(GOLDEN, "page_figures.json")))["items"]}
+    mib, gib = 2 ** 20, 2 ** 30
+    for key, unit in (("score_bytes_8k", mib), ("prob_bytes_4k", mib), ("prob_bytes_128k", gib)):
+        it = items[key]
+        assert it["N"] ** 2 * it["elem_bytes"] == it["value"] * unit
+    it = items["gemm_flops_per_exp_d128"]
+    # one score element costs one exponential; the FLOP convention gives it 4d flops
+    per_exp = oracle.flops_forward(1, 1, 1, it["d"], False)
+    assert per_exp == it["value"]
+    assert oracle.flops_backward(1, 1, 8, 64, True) == 2.5 * oracle.flops_forward(1, 1, 8, 64, True)
+
+
+# ---------------------------------------------------------------- input recipe
+
+def test_inputs_are_deterministic_and_bf16():
+    a = inputs.draw_bf16(1, 2, 16, 8, 0)
+    b = inputs.draw_bf16(1, 2, 16, 8, 0)
+    for x, y in zip(a, b):
+        assert x.dtype == torch.bfloat16
+        assert torch.equal(x, y)
+    c = inputs.draw_bf16(1, 2, 16, 8, 1)
+    assert not torch.equal(a[0], c[0])
+
+
+def test_fp8_quantisation_roundtrip():
+    x = inputs.draw_outlier_fp32(1, 2, 512, 64, 4)[0]
+    codes, delta = inputs.quantize_e4m3_per_tensor(x)
+    assert codes.dtype == torch.uint8
+    deq = inputs.e4m3_codes_to_fp32(codes) * delta
+    assert abs(float(deq.abs().max()) - float(x.abs().max())) <= 1e-6 * float(x.abs().max())
+    # e4m3 has 3 mantissa bits: relative rounding error <= 2^-4 on normals
+    big = x.abs() > 2 ** -6 * delta * 4
+    rel = ((deq - x).abs() / x.abs())[big]
+    assert float(rel.max()) <= 2 ** -4 + 1e-6
