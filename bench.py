@@ -1,0 +1,354 @@
+"""Throughput of exact attention fwd+bwd on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch: fa_fwd (forward
+kernel) then the three backward kernels (fa_bwd_preprocess, fa_bwd_main,
+fa_bwd_dq_convert, which together are fa_bwd).  Workload: causal bf16
+attention, B=2, H=16, N=8192, d=128, scale 1/sqrt(d), seeded N(0,1) inputs.
+FLOPs per step follow the convention fwd = 4 B H N^2 d (halved for causal),
+bwd = 2.5 x fwd.  Q, K, V and dO (256 MiB) exceed the 129 MB L2, so no flush.
+
+--gpus N > 1 runs under torchrun, one process per GPU: the attention path has
+no exchange step, so each rank runs an independent replica (weak scaling) and
+`value` is the work of all ranks over the slowest rank's time.
+
+--impl reference times the float64 CPU oracle on the host cores, one head of
+the same workload per step (a bounded sample).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(name="long_causal_B2_H16_N8192_d128", B=2, H=16, N=8192, d=128, causal=True, seed=3)
+METRIC = "attention fwd+bwd TFLOPS (bf16, causal, d=128, 1xGB300)"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def flops_step(B, H, N, d, causal):
+    fwd = 4.0 * B * H * N * N * d / (2.0 if causal else 1.0)
+    return fwd, 2.5 * fwd
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_76_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since those counters were taken."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        rec = json.load(f)
+    ent = rec.get("kernels", {}).get(kernel)
+    if not ent or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def cpu_oracle_sample(heads, N, d, causal, seed):
+    """Times the float64 oracle (forward + backward) on `heads` heads of the
+    workload; returns (seconds, flops of those heads)."""
+    import oracle
+    from exact_attention_76_gb300 import inputs
+
+    q, k, v, do = inputs.draw_bf16(1, heads, N, d, seed)
+    scale = 1.0 / math.sqrt(d)
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, causal, scale)
+    oracle.backward(q, k, v, do, causal, scale)
+    dt = time.perf_counter() - t0
+    f, b = flops_step(1, heads, N, d, causal)
+    return dt, f + b
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    W = WORKLOAD
+    for _ in range(args.warmup):
+        cpu_oracle_sample(1, W["N"], W["d"], W["causal"], W["seed"])
+    times, fl = [], 0.0
+    for _ in range(args.steps):
+        dt, fl = cpu_oracle_sample(1, W["N"], W["d"], W["causal"], W["seed"])
+        times.append(dt)
+    tot = sum(times)
+    value = fl * args.steps / tot / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": W["name"], "B": W["B"], "H": W["H"], "N": W["N"], "d": W["d"],
+                   "causal": W["causal"], "sample": "1 of 32 heads per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "one (batch, head) of the workload per step, fwd+bwd in float64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_76_gb300 import api, inputs
+    from exact_attention_76_gb300 import build as _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    W = WORKLOAD
+    B, H, N, d, causal = W["B"], W["H"], W["N"], W["d"], W["causal"]
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = inputs.draw_bf16(B, H, N, d, W["seed"])
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    Dv = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    acc = torch.empty((B, H, N, d), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    kernels = ["fa_fwd", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        api.fa_fwd(qd, kd, vd, causal, scale, o=o, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+        api.fa_bwd_preprocess(o, dod, D=Dv, dq_acc=acc)
+        if ev is not None:
+            ev[2].record(stream)
+        api.fa_bwd_main(qd, kd, vd, lse, dod, Dv, acc, causal, scale, dk=dk, dv=dv)
+        if ev is not None:
+            ev[3].record(stream)
+        api.fa_bwd_dq_convert(acc, scale, dq=dq)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if api.fa_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- timed region: K steps, CUDA events on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = start.elapsed_time(stop)
+    per_kernel = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j, n in enumerate(kernels)}
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    if api.fa_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    fwd_fl, bwd_fl = flops_step(B, H, N, d, causal)
+    step_fl = fwd_fl + bwd_fl
+    ms_step = ms_total / args.steps
+    value = world * step_fl * args.steps / (ms_total * 1e-3) / 1e12
+
+    # ---- end to end through the same API with pinned host buffers
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for h, dvc in ((hq, qd), (hk, kd), (hv, vd), (hdo, dod)):
+            dvc.copy_(h, non_blocking=True)
+        step()
+        for h, dvc in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+            h.copy_(dvc, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e_value = world * step_fl * e2e_steps / (ms_e2e * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = measured_peaks()
+    fl_per_kernel = {"fa_fwd": fwd_fl, "fa_bwd_main": bwd_fl}
+    dom = max(per_kernel, key=per_kernel.get)
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    if dom in fl_per_kernel:
+        achieved = fl_per_kernel[dom] / (per_kernel[dom] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(dom), "kernel": dom,
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a multi-ms step)"}
+    else:
+        roof = {"bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": None,
+                "traffic": recorded_traffic(dom), "kernel": dom}
+    # secondary figures: every kernel's share and the memory-bound kernels' GB/s
+    rows = B * H * N
+    hbm_bytes = {"fa_bwd_preprocess": rows * (2 * d * 2 + 4 + 4 * d), "fa_bwd_dq_convert": rows * (4 * d + 2 * d)}
+    kernel_stats = {}
+    for n, ms in per_kernel.items():
+        ent = {"ms": ms, "share": ms / sum(per_kernel.values())}
+        if n in fl_per_kernel:
+            ent["tflops"] = fl_per_kernel[n] / (ms * 1e-3) / 1e12
+            ent["frac_of_bf16_sustained"] = ent["tflops"] / peak
+        if n in hbm_bytes:
+            ent["gbs"] = hbm_bytes[n] / (ms * 1e-3) / 1e9
+            ent["frac_of_hbm"] = ent["gbs"] / peaks["hbm_gbs"]
+        kernel_stats[n] = ent
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": W["name"], "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "scale": "1/sqrt(d)", "l2": "no flush: Q,K,V,dO are 256 MiB, larger than L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "kernels": kernel_stats,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads = 2
+        dt, fl = cpu_oracle_sample(heads, N, d, causal, W["seed"])
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{heads} of {B * H} heads, fwd+bwd in float64 ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,148 @@
+"""Python face of the C ABI (include/fa.h), one function per entry point and
+with the same names.  PyTorch supplies device memory and the stream; every
+step of the computation runs in the library's CUDA kernels.
+
+Tensors are CUDA, contiguous, [B, H, N, d]; bf16 unless stated; statistics
+([B, H, N]) are fp32.  Outputs may be passed in (pre-allocated) or are
+allocated here with torch.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor):
+    return t.data_ptr()
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def fa_fwd(q, k, v, causal: bool, scale: float, o=None, lse=None, stream=None):
+    """O = softmax(scale QK^T [+ causal mask]) V and L = logsumexp of the scaled logits."""
+    lib = _lib.load()
+    B, H, N, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, (B, H, N, d))
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check(o, "o", torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    _lib.check("fa_fwd", lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                                    float(scale), _stream_ptr(stream)))
+    return o, lse
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dO, causal: bool, scale: float, dq=None, dk=None, dv=None, workspace=None,
+           stream=None):
+    """dQ, dK, dV of O = softmax(scale QK^T [+mask]) V for upstream gradient dO."""
+    lib = _lib.load()
+    B, H, N, d = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO")):
+        _check(t, n, torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, torch.bfloat16, (B, H, N, d))
+    need = fa_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8)
+    _lib.check("fa_bwd", lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), _ptr(workspace), workspace.numel(), B, H, N, d, int(bool(causal)),
+                                    float(scale), _stream_ptr(stream)))
+    return dq, dk, dv
+
+
+def fa_bwd_preprocess(o, dO, D=None, dq_acc=None, stream=None):
+    """D = rowsum(dO * O) in fp32 and a zeroed fp32 dQ accumulator."""
+    lib = _lib.load()
+    B, H, N, d = o.shape
+    _check(o, "o", torch.bfloat16)
+    _check(dO, "dO", torch.bfloat16, (B, H, N, d))
+    D = torch.empty((B, H, N), dtype=torch.float32, device=o.device) if D is None else D
+    dq_acc = torch.empty((B, H, N, d), dtype=torch.float32, device=o.device) if dq_acc is None else dq_acc
+    _check(D, "D", torch.float32, (B, H, N))
+    _check(dq_acc, "dq_acc", torch.float32, (B, H, N, d))
+    _lib.check("fa_bwd_preprocess", lib.fa_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(D), _ptr(dq_acc), B, H, N, d,
+                                                          _stream_ptr(stream)))
+    return D, dq_acc
+
+
+def fa_bwd_main(q, k, v, lse, dO, D, dq_acc, causal: bool, scale: float, dk=None, dv=None, stream=None):
+    """dK, dV (bf16) and dS K added into dq_acc (fp32)."""
+    lib = _lib.load()
+    B, H, N, d = q.shape
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _lib.check("fa_bwd_main", lib.fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(dO), _ptr(D),
+                                              _ptr(dq_acc), _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)),
+                                              float(scale), _stream_ptr(stream)))
+    return dk, dv
+
+
+def fa_bwd_dq_convert(dq_acc, scale: float, dq=None, stream=None):
+    """dQ = bf16(scale * dq_acc)."""
+    lib = _lib.load()
+    B, H, N, d = dq_acc.shape
+    _check(dq_acc, "dq_acc", torch.float32)
+    dq = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dq_acc.device) if dq is None else dq
+    _lib.check("fa_bwd_dq_convert", lib.fa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, H, N, d, float(scale),
+                                                          _stream_ptr(stream)))
+    return dq
+
+
+def fa_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, causal: bool, scale: float, o=None, lse=None,
+               stream=None):
+    """FP8 forward: q8/k8/v8 are e4m3 codes (torch.uint8 or float8_e4m3fn), descales are
+    1-element fp32 CUDA tensors; returns bf16 O and fp32 L."""
+    lib = _lib.load()
+    B, H, N, d = q8.shape
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise TypeError(f"{n}: expected e4m3 codes")
+        _check(t, n, t.dtype, (B, H, N, d))
+    for t, n in ((descale_q, "descale_q"), (descale_k, "descale_k"), (descale_v, "descale_v")):
+        _check(t, n, torch.float32)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _lib.check("fa_fwd_fp8", lib.fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(descale_q), _ptr(descale_k),
+                                            _ptr(descale_v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                                            float(scale), _stream_ptr(stream)))
+    return o, lse
+
+
+def fa_status_string(status: int) -> str:
+    return _lib.load().fa_status_string(int(status)).decode()
+
+
+def fa_device_error(stream=None) -> int:
+    """Synchronises the stream; returns the status code (0 = FA_OK, 5 = FA_ERR_TIMEOUT)."""
+    return int(_lib.load().fa_device_error(_stream_ptr(stream)))
+
+
+def fa_debug_wait_timeout(limit_us: int, stream=None) -> int:
+    return int(_lib.load().fa_debug_wait_timeout(int(limit_us), _stream_ptr(stream)))

@@ -1,0 +1,249 @@
+// The C ABI declared in include/fa.h: argument checks, TMA tensor-map
+// encoding, and the launch sequence of each entry point on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa_common.cuh"
+#include "fa_host.h"
+
+namespace fa {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn resolve_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_shape(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh * N > (1LL << 31) / 1 || bh > (1LL << 30)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status check_scale(float scale) {
+  return (std::isfinite(scale) && scale > 0.f) ? FA_OK : FA_ERR_INVALID_ARG;
+}
+
+fa_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return (major == 10 && minor == 3) ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+template <typename... P>
+fa_status check_ptrs(P... ptrs) {
+  const void* list[] = {static_cast<const void*>(ptrs)...};
+  for (const void* p : list)
+    if (p == nullptr) return FA_ERR_INVALID_ARG;
+  for (const void* p : list)
+    if (!aligned16(p)) return FA_ERR_ALIGNMENT;
+  return FA_OK;
+}
+
+size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
+
+// ---------------------------------------------------------------- timeout hook
+
+__device__ uint32_t g_err_probe;
+
+__global__ void timeout_probe_kernel(long long limit_cycles) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  // Nothing ever arrives on `bar`: the wait below must run out and report.
+  const long long t0 = clock64();
+  while (!mbar_try_wait(&bar, 0)) {
+    if (clock64() - t0 > limit_cycles) {
+      atomicOr(&g_err_probe, FA_DEVERR_TIMEOUT);
+      return;
+    }
+  }
+}
+
+}  // namespace
+
+bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, int cols, int N, int BH, int box_cols,
+                     int box_rows) {
+  EncodeTiledFn enc = resolve_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * elem_bytes,
+                                 static_cast<cuuint64_t>(cols) * elem_bytes * static_cast<cuuint64_t>(N)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+fa_status launch_timeout_probe(unsigned int limit_us, cudaStream_t stream) {
+  int dev = 0, khz = 2000000;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+  const long long cycles = static_cast<long long>(limit_us) * (khz / 1000);
+  timeout_probe_kernel<<<1, 32, 0, stream>>>(cycles);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+uint32_t probe_take_error(cudaStream_t s) {
+  uint32_t v = 0, zero = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_err_probe, sizeof(v), 0, cudaMemcpyDeviceToHost, s);
+  cudaStreamSynchronize(s);
+  cudaMemcpyToSymbolAsync(g_err_probe, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+  cudaStreamSynchronize(s);
+  return v;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 int causal, float scale, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(q, k, v, o, lse)) != FA_OK) return st;
+  if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_device()) != FA_OK) return st;
+  FwdArgs a{q, k, v, o, lse, nullptr, nullptr, nullptr, B, H, N, d, causal, scale};
+  return launch_fwd_bf16(a, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_shape(B, H, N, d) != FA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return round16(rows * sizeof(float)) + rows * d * sizeof(float);
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, int B, int H, int N, int d,
+                            void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(o, dO, D, dq_acc)) != FA_OK) return st;
+  if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if ((st = check_device()) != FA_OK) return st;
+  return launch_bwd_preprocess(o, dO, D, dq_acc, static_cast<long long>(B) * H * N, d,
+                               static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* lse, const void* dO,
+                      const float* D, float* dq_acc, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                      float scale, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(q, k, v, lse, dO, D, dq_acc, dk, dv)) != FA_OK) return st;
+  if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_device()) != FA_OK) return st;
+  BwdArgs a{q, k, v, lse, dO, D, dq_acc, dk, dv, B, H, N, d, causal, scale};
+  return launch_bwd_main(a, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(dq_acc, dq)) != FA_OK) return st;
+  if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if ((st = check_device()) != FA_OK) return st;
+  return launch_bwd_dq_convert(dq_acc, dq, static_cast<long long>(B) * H * N, d, scale,
+                               static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 int causal, float scale, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(q, k, v, o, lse, dO, dq, dk, dv)) != FA_OK) return st;
+  if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_bwd_workspace_size(B, H, N, d);
+  if (workspace == nullptr || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
+  if ((st = check_device()) != FA_OK) return st;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  float* Dvec = static_cast<float*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round16(rows * sizeof(float)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = launch_bwd_preprocess(o, dO, Dvec, dq_acc, static_cast<long long>(rows), d, s)) != FA_OK) return st;
+  BwdArgs a{q, k, v, lse, dO, Dvec, dq_acc, dk, dv, B, H, N, d, causal, scale};
+  if ((st = launch_bwd_main(a, s)) != FA_OK) return st;
+  return launch_bwd_dq_convert(dq_acc, dq, static_cast<long long>(rows), d, scale, s);
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale_q,
+                     const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H, int N,
+                     int d, int causal, float scale, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(q8, k8, v8, o, lse)) != FA_OK) return st;
+  if (descale_q == nullptr || descale_k == nullptr || descale_v == nullptr) return FA_ERR_INVALID_ARG;
+  if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_device()) != FA_OK) return st;
+  FwdArgs a{q8, k8, v8, o, lse, descale_q, descale_k, descale_v, B, H, N, d, causal, scale};
+  return launch_fwd_fp8(a, static_cast<cudaStream_t>(stream));
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer, non-positive size or bad scale";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim or device not supported";
+    case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT: a pointer is not 16-byte aligned";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: kernel launch or tensor-map encoding failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait ran past its limit";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "unknown fa_status";
+}
+
+fa_status fa_device_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_LAUNCH;
+  uint32_t e = fwd_bf16_take_error(s) | bwd_take_error(s) | probe_take_error(s);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_LAUNCH;
+  if (e & FA_DEVERR_TIMEOUT) return FA_ERR_TIMEOUT;
+  if (e != 0) return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
+fa_status fa_debug_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return FA_ERR_INVALID_ARG;
+  fa_status st;
+  if ((st = check_device()) != FA_OK) return st;
+  return launch_timeout_probe(limit_us, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,538 @@
+// Backward attention kernels for sm_103a.
+//
+// The chain rule for O = softmax(S) V, S = scale * Q K^T ("FLASH-ATTN",
+// FlashAttention-2 > Background): dV = P^T dO, dP = dO V^T, dS = P o (dP - D)
+// with D_i = sum_j P_ij dP_ij (the row-softmax Jacobian), dQ = scale dS K,
+// dK = scale dS^T Q.  P is rebuilt block by block from the saved L
+// (P_ij = exp(S_ij - L_i)) instead of being stored ("FLASH-ATTN",
+// FlashAttention > Tiling and Recomputation: selective recomputation).
+//
+// Three kernels:
+//  1. fa_bwd_preprocess: D_i = sum_k dO_ik O_ik (equal to sum_j P_ij dP_ij
+//     because O = P V) and zeros for the fp32 dQ accumulator.  HBM bound.
+//  2. fa_bwd_main_kernel: one CTA per 128-key block of a head, query blocks
+//     inner ("FLASH-ATTN", FlashAttention-2 > Parallelism: column blocks get
+//     their own thread blocks and meet only through atomic adds to dQ).  The
+//     five products run on tcgen05 with accumulators in TMEM:
+//       S^T  = K Q_i^T        (smem x smem)        -> TMEM
+//       dP^T = V dO_i^T       (smem x smem)        -> TMEM
+//       dV  += P^T dO_i       (P^T from TMEM)      -> TMEM, whole loop
+//       dK  += dS^T Q_i       (dS^T from smem)     -> TMEM, whole loop
+//       dQ_i = dS K           (dS^T read MN-major) -> TMEM, then fp32 atomics
+//     Causal: query blocks below the key block are skipped; only the
+//     diagonal block applies the element mask.
+//  3. fa_bwd_dq_convert: dQ = bf16(scale * dQ_acc).  HBM bound.
+//
+// Roles of fa_bwd_main_kernel (320 threads):
+//  warps 0-3  thread r owns key row r: P^T = exp2(S^T c - L_i log2 e) into
+//             TMEM (bf16, over S^T), then dS^T = P^T o (dP^T - D_i) into smem;
+//             finally writes dV.
+//  warps 4-7  thread r owns query row r of the current block: reads dQ_i
+//             from TMEM and adds it into the fp32 accumulator; finally
+//             writes dK = scale * acc.
+//  warp 8     TMA producer: K and V once, Q_i and dO_i into two stages, and
+//             L_i, D_i into shared memory.
+//  warp 9     TMEM allocation and the single MMA-issuing thread.
+#include <cuda_bf16.h>
+
+#include "fa_common.cuh"
+#include "fa_host.h"
+
+namespace fa {
+
+namespace {
+
+__device__ uint32_t g_err_bwd;
+
+constexpr int kThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- preprocess
+
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ o,
+                                                                const __nv_bfloat16* __restrict__ dout,
+                                                                float* __restrict__ dvec,
+                                                                float* __restrict__ dq_acc, long long rows) {
+  constexpr int kLanesPerRow = D / 8;  // each lane: 8 bf16 = 16 bytes of O and of dO
+  constexpr int kRowsPerBlock = 256 / kLanesPerRow;
+  const int sub = threadIdx.x % kLanesPerRow;
+  const long long row = static_cast<long long>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kLanesPerRow;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + sub);
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + sub);
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fa_ = __bfloat1622float2(pa[i]);
+      const float2 fb_ = __bfloat1622float2(pb[i]);
+      acc = fmaf(fa_.x, fb_.x, acc);
+      acc = fmaf(fa_.y, fb_.y, acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + row * D) + 2 * sub;
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) dvec[row] = acc;
+}
+
+// ---------------------------------------------------------------- convert
+
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __restrict__ acc,
+                                                                __nv_bfloat16* __restrict__ dq, long long n8,
+                                                                float scale) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+    uint4 r;
+    r.x = pack_bf16x2(a.x * scale, a.y * scale);
+    r.y = pack_bf16x2(a.z * scale, a.w * scale);
+    r.z = pack_bf16x2(b.x * scale, b.y * scale);
+    r.w = pack_bf16x2(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = r;
+  }
+}
+
+// ---------------------------------------------------------------- main
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = 128 * D * 2;   // one 128-row bf16 tile
+  static constexpr int kColBlocks = D / 64;        // 128-byte column blocks per row
+  static constexpr int kBlockBytes = 128 * 128;
+  static constexpr int kDsBytes = 128 * 128 * 2;   // dS^T, 128 keys x 128 queries
+  // shared memory layout (offsets from a 1024-aligned base)
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffQ = kOffV + kTileBytes;           // 2 stages
+  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;      // 2 stages
+  static constexpr int kOffDS = kOffDO + 2 * kTileBytes;
+  static constexpr int kOffL = kOffDS + kDsBytes;            // float [2][128]
+  static constexpr int kOffDv = kOffL + 2 * 128 * 4;         // float [2][128]
+  static constexpr int kOffBar = kOffDv + 2 * 128 * 4;
+  static constexpr int kSmemBytes = kOffBar + 256;
+  // TMEM columns
+  static constexpr uint32_t kTmDV = 0;
+  static constexpr uint32_t kTmDK = D;
+  static constexpr uint32_t kTmS = 2 * D;
+  static constexpr uint32_t kTmDP = 2 * D + 128;
+  static constexpr uint32_t kTmDQ = (D == 128) ? kTmDP : 2 * D + 256;  // aliases dP^T when D = 128
+  static constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);
+  static constexpr uint32_t kIdescKM = idesc_bf16(128, D, false, true);
+  static constexpr uint32_t kIdescMM = idesc_bf16(128, D, true, true);
+};
+
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t qdo_full[2];
+  uint64_t qdo_empty[2];
+  uint64_t ld_full[2];
+  uint64_t ld_empty[2];
+  uint64_t s_full, p_ready, dp_full, ds_ready, dv_done, ds_free, dq_full, dq_free, acc_done, drain;
+  uint32_t tmem_base;
+  CtaAbort abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                       const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                       const float* __restrict__ lse, const float* __restrict__ dvec, float* __restrict__ dq_acc,
+                       __nv_bfloat16* __restrict__ dk_out, __nv_bfloat16* __restrict__ dv_out, int BH, int N,
+                       int causal, float scale, float scale_log2) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  static_assert(sizeof(BwdBars) <= 256, "barrier block");
+  BwdBars& sh = *reinterpret_cast<BwdBars*>(smem + C::kOffBar);
+  // The tile offsets assume a 1024-byte aligned base (the swizzle atoms).
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(&g_err_bwd, 2u);
+    return;
+  }
+  // A wait of an earlier CTA ran out: the launch is already failed, stop here
+  // (the word stays set until fa_device_error reads and clears it).
+  if (*reinterpret_cast<volatile uint32_t*>(&g_err_bwd) & FA_DEVERR_TIMEOUT) return;
+  float* s_lse2 = reinterpret_cast<float*>(smem + C::kOffL);
+  float* s_dvec = reinterpret_cast<float*>(smem + C::kOffDv);
+
+  const int warp = warp_id();
+  const int n_blk = (N + 127) / 128;
+  const int item = static_cast<int>(blockIdx.x);
+  const int kb = item / BH;  // key block; ascending = most work first under a causal mask
+  const int bh = item % BH;
+  const int i_begin = causal ? kb : 0;
+  const int n_it = n_blk - i_begin;
+
+  if (threadIdx.x == 0) {
+    sh.abort.flag = 0;
+    mbar_init(&sh.kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.qdo_full[s], 1);
+      mbar_init(&sh.qdo_empty[s], 1);
+      mbar_init(&sh.ld_full[s], 32);
+      mbar_init(&sh.ld_empty[s], 128);
+    }
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.p_ready, 128);
+    mbar_init(&sh.dp_full, 1);
+    mbar_init(&sh.ds_ready, 128);
+    mbar_init(&sh.dv_done, 1);
+    mbar_init(&sh.ds_free, 1);
+    mbar_init(&sh.dq_full, 1);
+    mbar_init(&sh.dq_free, 128);
+    mbar_init(&sh.acc_done, 1);
+    mbar_init(&sh.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) tmem_alloc(&sh.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    const int lane = lane_id();
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_do);
+      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kTileBytes);
+      for (int cb = 0; cb < C::kColBlocks; ++cb) {
+        tma_load_3d(smem + C::kOffK + cb * C::kBlockBytes, &map_k, cb * 64, kb * 128, bh, &sh.kv_full);
+        tma_load_3d(smem + C::kOffV + cb * C::kBlockBytes, &map_v, cb * 64, kb * 128, bh, &sh.kv_full);
+      }
+    }
+    int issued[2] = {0, 0};  // Q/dO loads issued per stage (lane 0)
+    for (int it = 0; it < n_it; ++it) {
+      if (__shfl_sync(0xffffffffu, sh.abort.flag, 0)) break;  // one decision for the whole warp
+      const int st = it & 1;
+      const int use = it >> 1;
+      const int qrow0 = (i_begin + it) * 128;
+      bool ok = true;
+      if (lane == 0) {
+        if (use > 0) ok = mbar_wait(&sh.qdo_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd);
+        if (ok) {
+          mbar_arrive_expect_tx(&sh.qdo_full[st], 2 * C::kTileBytes);
+          for (int cb = 0; cb < C::kColBlocks; ++cb) {
+            tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * 64, qrow0, bh,
+                        &sh.qdo_full[st]);
+            tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, bh,
+                        &sh.qdo_full[st]);
+          }
+          ++issued[st];
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      if (use > 0 && !mbar_wait(&sh.ld_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd)) break;
+      // L in log2 units (+inf past the end: P = 0 there) and D, 4 rows per lane.
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = lane * 4 + u;
+        const int qg = qrow0 + r;
+        float l2 = INFINITY, dd = 0.f;
+        if (qg < N) {
+          l2 = __ldg(lse + static_cast<size_t>(bh) * N + qg) * kLog2e;
+          dd = __ldg(dvec + static_cast<size_t>(bh) * N + qg);
+        }
+        s_lse2[st * 128 + r] = l2;
+        s_dvec[st * 128 + r] = dd;
+      }
+      mbar_arrive(&sh.ld_full[st]);
+    }
+    if (lane == 0 && sh.abort.flag) {
+      // Let every copy still in flight land before the CTA's memory goes away.
+      mbar_wait_drain(&sh.kv_full, 0, &g_err_bwd);
+      for (int s2 = 0; s2 < 2; ++s2)
+        if (issued[s2] > 0) mbar_wait_drain(&sh.qdo_full[s2], (issued[s2] - 1) & 1, &g_err_bwd);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      const uint32_t sm = smem_u32(smem);
+      const uint32_t k_addr = sm + C::kOffK, v_addr = sm + C::kOffV, ds_addr = sm + C::kOffDS;
+      bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_err_bwd);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it & 1;
+        const uint32_t q_addr = sm + C::kOffQ + st * C::kTileBytes;
+        const uint32_t do_addr = sm + C::kOffDO + st * C::kTileBytes;
+        ok = mbar_wait(&sh.qdo_full[st], (it >> 1) & 1, &sh.abort, &g_err_bwd);
+        if (ok && it > 0) ok = mbar_wait(&sh.dv_done, (it - 1) & 1, &sh.abort, &g_err_bwd);  // P^T read
+        if (!ok) break;
+        tc_fence_after();
+        // S^T = K Q_i^T
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::kTmS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
+                      C::kIdescKK, kk > 0);
+        }
+        tc_commit(&sh.s_full);
+        if (D == 128 && it > 0) {  // dP^T shares columns with dQ_(i-1)
+          ok = mbar_wait(&sh.dq_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // dP^T = V dO_i^T
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::kTmDP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
+                      C::kIdescKK, kk > 0);
+        }
+        tc_commit(&sh.dp_full);
+        // dV += P^T dO_i
+        ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
+        if (!ok) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmS + kk * 8, sdesc_sw128(do_addr + kk * 2048, C::kBlockBytes, 1024),
+                      C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&sh.dv_done);
+        // dK += dS^T Q_i ; dQ_i = dS K
+        ok = mbar_wait(&sh.ds_ready, it & 1, &sh.abort, &g_err_bwd);
+        if (!ok) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::kTmDK, sdesc_sw128(ds_addr + off, 16, 1024),
+                      sdesc_sw128(q_addr + kk * 2048, C::kBlockBytes, 1024), C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (D == 64 && it > 0) {  // separate dQ columns: only the previous read-out must be done
+          ok = mbar_wait(&sh.dq_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ss(tmem + C::kTmDQ, sdesc_sw128(ds_addr + kk * 2048, C::kBlockBytes, 1024),
+                      sdesc_sw128(k_addr + kk * 2048, C::kBlockBytes, 1024), C::kIdescMM, kk > 0);
+        tc_commit(&sh.dq_full);
+        tc_commit(&sh.ds_free);
+        tc_commit(&sh.qdo_empty[st]);
+      }
+      if (ok) tc_commit(&sh.acc_done);
+      tc_commit(&sh.drain);
+      mbar_wait_drain(&sh.drain, 0, &g_err_bwd);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P and dS (key rows)
+    const int r = threadIdx.x;  // key row within the block == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int kg = kb * 128 + r;
+    uint8_t* ds_row = smem + C::kOffDS + r * 128;
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it & 1;
+      ok = mbar_wait(&sh.ld_full[st], (it >> 1) & 1, &sh.abort, &g_err_bwd) &&
+           mbar_wait(&sh.s_full, it & 1, &sh.abort, &g_err_bwd);
+      if (!ok) break;
+      tc_fence_after();
+      const float* l2 = s_lse2 + st * 128;
+      const float* dd = s_dvec + st * 128;
+      const bool diag = causal && (i_begin + it == kb);
+      float p[128];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kTmS + cc * 32, rr);
+        tmem_ld_wait(rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int q = cc * 32 + i;
+          float x = ex2_approx(fmaf(__uint_as_float(rr[i]), scale_log2, -l2[q]));
+          if (diag && q < r) x = 0.f;  // query before key: masked
+          p[q] = x;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pw[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(p[64 * h + 2 * i], p[64 * h + 2 * i + 1]);
+        tmem_st32(tmem + lane_base + C::kTmS + h * 32, pw);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sh.p_ready);
+      ok = mbar_wait(&sh.dp_full, it & 1, &sh.abort, &g_err_bwd);
+      if (ok && it > 0) ok = mbar_wait(&sh.ds_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kTmDP + cc * 32, rr);
+        tmem_ld_wait(rr);
+        // 32 queries = two 16-byte chunks of 8 in column block cc/2
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int q0 = cc * 32 + 2 * i;
+          const float a = p[q0] * (__uint_as_float(rr[2 * i]) - dd[q0]);
+          const float b = p[q0 + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[q0 + 1]);
+          w[i] = pack_bf16x2(a, b);
+        }
+        uint8_t* blk = ds_row + (cc >> 1) * C::kBlockBytes;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + c4);
+          *reinterpret_cast<uint4*>(blk + ((chunk ^ swz) << 4)) =
+              make_uint4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+        }
+      }
+      // generic-proxy stores -> visible to the tensor core's async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(&sh.ds_ready);
+      mbar_arrive(&sh.ld_empty[st]);
+    }
+    // dV = sum_i P_i^T dO_i
+    if (ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd)) {
+      tc_fence_after();
+      const bool store = kg < N;
+      __nv_bfloat16* dst = dv_out + (static_cast<size_t>(bh) * N + (store ? kg : 0)) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kTmDV + cc, rr);
+        tmem_ld_wait(rr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
+        if (store) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ read-out (query rows), dK epilogue
+    const int r = threadIdx.x - 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      ok = mbar_wait(&sh.dq_full, it & 1, &sh.abort, &g_err_bwd);
+      if (!ok) break;
+      tc_fence_after();
+      float v[D];
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kTmDQ + cc * 32, rr);
+        tmem_ld_wait(rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[cc * 32 + i] = __uint_as_float(rr[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.dq_free);
+      const int qg = (i_begin + it) * 128 + r;
+      if (qg < N) {
+        float4* dst = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * N + qg) * D);
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i)
+          atomicAdd(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+      }
+    }
+    // dK = scale * sum_i dS_i^T Q_i
+    if (ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd)) {
+      tc_fence_after();
+      const int kg = kb * 128 + r;
+      const bool store = kg < N;
+      __nv_bfloat16* dst = dk_out + (static_cast<size_t>(bh) * N + (store ? kg : 0)) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_base + C::kTmDK + cc, rr);
+        tmem_ld_wait(rr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * scale, __uint_as_float(rr[2 * i + 1]) * scale);
+        if (store) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_rows_map(&mq, a.q, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mk, a.k, 2, D, a.N, BH, 64, 128) ||
+      !encode_rows_map(&mv, a.v, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdo, a.dO, 2, D, a.N, BH, 64, 128))
+    return FA_ERR_LAUNCH;
+  auto kern = fa_bwd_main_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  const int n_blk = (a.N + 127) / 128;
+  dim3 grid(static_cast<unsigned>(n_blk * BH));
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a.lse, a.D, a.dq_acc,
+                                                   static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv),
+                                                   BH, a.N, a.causal, a.scale, a.scale * kLog2e);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+fa_status launch_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, long long rows, int d,
+                                cudaStream_t stream) {
+  const int rows_per_block = 256 / (d / 8);
+  const long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+  if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if (d == 64)
+    fa_bwd_preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), D, dq_acc, rows);
+  else
+    fa_bwd_preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), D, dq_acc, rows);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+fa_status launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
+  return a.d == 64 ? launch_bwd_main_impl<64>(a, stream) : launch_bwd_main_impl<128>(a, stream);
+}
+
+fa_status launch_bwd_dq_convert(const float* dq_acc, void* dq, long long rows, int d, float scale,
+                                cudaStream_t stream) {
+  const long long n8 = rows * d / 8;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = (n8 + 255) / 256;
+  const long long cap = static_cast<long long>(sms) * 8;  // grid-stride beyond 8 waves of 256 threads
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  fa_bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(dq), n8, scale);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+uint32_t bwd_take_error(cudaStream_t s) {
+  uint32_t v = 0, zero = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_err_bwd, sizeof(v), 0, cudaMemcpyDeviceToHost, s);
+  cudaStreamSynchronize(s);
+  cudaMemcpyToSymbolAsync(g_err_bwd, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+  cudaStreamSynchronize(s);
+  return v;
+}
+
+}  // namespace fa

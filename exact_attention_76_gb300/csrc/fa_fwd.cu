@@ -1,0 +1,427 @@
+// Forward attention kernel for sm_103a (bf16 and e4m3 inputs).
+//
+// What it computes ("FLASH-ATTN", FlashAttention-2 > FlashAttention-2): for a
+// block of query rows, a loop over key/value blocks keeps a running row max m,
+// a running row sum l of exp(S - m) and an UNSCALED output accumulator
+// O~ = sum_j exp(S_j - m) V_j; O = diag(l)^-1 O~ and L = m + log(l) are formed
+// once after the loop.  Fully masked blocks of a causal row block are never
+// visited and only the diagonal block applies the element mask (same
+// section).  Query blocks are independent thread blocks (> Parallelism).
+//
+// How it maps to the SM (one CTA = 256 query rows of one (batch, head)):
+//  * warps 0-3 and 4-7: two softmax warpgroups, one per 128-row query tile;
+//    thread r of a warpgroup owns row r (TMEM lane r);
+//  * warp 8: TMA producer -- the two Q tiles once, then K_j and V_j into a
+//    ring of shared-memory slots guarded by full/empty mbarriers (the
+//    producer/consumer split of "FLASH-ATTN", FlashAttention-3 >
+//    Producer-Consumer asynchrony);
+//  * warp 9: allocates TMEM and, from one thread, issues every tcgen05.mma:
+//    S_t = Q_t K_j^T (both operands in shared memory) and O_t += P_t V_j with
+//    P_t read from TMEM, where the softmax warpgroup wrote it over S_t.
+// The MMA order per key block j is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
+// each warpgroup's softmax overlaps the other tile's two products (the
+// ping-pong of two consumer warpgroups, "FLASH-ATTN", FlashAttention-3).
+//
+// Softmax works in the log2 domain: x = S * (scale * log2 e) with one FMA, then
+// ex2.  The reference maximum m_used is raised only when a block's maximum
+// exceeds it by more than TAU (8 for bf16, i.e. values up to 2^8 before a
+// rescale; 0 for e4m3, whose P must stay <= 1); raising it rescales l and
+// the warpgroup's own O row in TMEM.  Any TAU gives the same exact result.
+//
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+#include <cuda_bf16.h>
+
+#include "fa_common.cuh"
+#include "fa_host.h"
+
+namespace fa {
+
+namespace {
+
+__device__ uint32_t g_err_fwd;
+
+constexpr int kThreads = 320;
+constexpr int kBM = 128;  // query rows per tile (one TMEM lane each)
+constexpr int kBN = 128;  // keys per key/value block
+
+template <int D, bool FP8>
+struct FwdCfg {
+  static constexpr int kElemBytes = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElemBytes;     // bytes of one row of Q/K/V
+  static constexpr int kColBlocks = kRowBytes / 128;   // 128-byte column blocks
+  static constexpr int kBoxCols = 128 / kElemBytes;    // elements per TMA box row
+  static constexpr int kTileBytes = 128 * kRowBytes;   // one 128-row tile
+  static constexpr int kBlockBytes = 128 * 128;        // one column block of a tile
+  static constexpr int kSlots = (kTileBytes >= 32768) ? 4 : 8;
+  static constexpr int kSmemBytes = 2 * kTileBytes + kSlots * kTileBytes + 1024;
+  static constexpr int kKPerMma = FP8 ? 32 : 16;       // K extent of one MMA
+  static constexpr int kQKSteps = kRowBytes / 32;      // MMAs for S = Q K^T
+  static constexpr int kPVSteps = kBN / kKPerMma;      // MMAs for O += P V
+  static constexpr float kTauLog2 = FP8 ? 0.0f : 8.0f;
+  static constexpr float kPScale = FP8 ? 256.0f : 1.0f;
+  static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(128, kBN, false, false) : idesc_bf16(128, kBN, false, false);
+  static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(kColBlocks >= 1, "row must fill a 128-byte swizzle row");
+};
+
+struct FwdSmem {
+  uint64_t q_full;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  CtaAbort abort;
+};
+
+__device__ __forceinline__ void issue_mma(bool fp8, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (fp8) mma_f8_ss(d, a, b, idesc, acc);
+  else mma_bf16_ss(d, a, b, idesc, acc);
+}
+__device__ __forceinline__ void issue_mma_ts(bool fp8, uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+  if (fp8) mma_f8_ts(d, a, b, idesc, acc);
+  else mma_bf16_ts(d, a, b, idesc, acc);
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, __nv_bfloat16* __restrict__ out_o,
+                  float* __restrict__ out_lse, const float* __restrict__ descale_q,
+                  const float* __restrict__ descale_k, const float* __restrict__ descale_v, int BH, int N,
+                  int causal, float scale_log2) {
+  using C = FwdCfg<D, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ FwdSmem sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_q = smem;                       // two Q tiles
+  uint8_t* s_kv = smem + 2 * C::kTileBytes;  // ring of K/V slots
+
+  // A wait of an earlier CTA ran out: the launch is already failed, stop here
+  // (the word stays set until fa_device_error reads and clears it).
+  if (*reinterpret_cast<volatile uint32_t*>(&g_err_fwd) & FA_DEVERR_TIMEOUT) return;
+  const int warp = warp_id();
+  const int n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
+  // Longest rows first: under a causal mask the last query blocks of every
+  // head see the most keys, so they take the lowest block indices and are
+  // dispatched first.
+  const int item = static_cast<int>(blockIdx.x);
+  const int qb = causal ? (n_qblk - 1 - item / BH) : item / BH;
+  const int bh = item % BH;
+  const int q0 = qb * 2 * kBM;
+  const int n_kv_all = (N + kBN - 1) / kBN;
+  int n_t[2];
+  for (int t = 0; t < 2; ++t) {
+    const int row0 = q0 + t * kBM;
+    if (row0 >= N) n_t[t] = 0;
+    else n_t[t] = causal ? min(n_kv_all, row0 / kBN + 1) : n_kv_all;
+  }
+  const int n_max = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    sh.abort.flag = 0;
+    mbar_init(&sh.q_full, 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&sh.kv_full[s], 1);
+      mbar_init(&sh.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sh.s_full[t], 1);
+      mbar_init(&sh.p_full[t], kBM);
+      mbar_init(&sh.o_done[t], 1);
+    }
+    mbar_init(&sh.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) tmem_alloc(&sh.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      mbar_arrive_expect_tx(&sh.q_full, 2 * C::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_load_3d(s_q + t * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * C::kBoxCols, q0 + t * kBM, bh,
+                      &sh.q_full);
+      int issued = 0;
+      for (int j = 0; j < n_max && !sh.abort.flag; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
+          const int slot = issued % C::kSlots;
+          const int round = issued / C::kSlots;
+          if (round > 0 && !mbar_wait(&sh.kv_empty[slot], (round - 1) & 1, &sh.abort, &g_err_fwd)) break;
+          mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
+          const CUtensorMap* m = kv == 0 ? &map_k : &map_v;
+          for (int cb = 0; cb < C::kColBlocks; ++cb)
+            tma_load_3d(s_kv + slot * C::kTileBytes + cb * C::kBlockBytes, m, cb * C::kBoxCols, j * kBN, bh,
+                        &sh.kv_full[slot]);
+          ++issued;
+        }
+      }
+      if (sh.abort.flag) {
+        // Let every copy still in flight land before the CTA's memory goes away.
+        mbar_wait_drain(&sh.q_full, 0, &g_err_fwd);
+        for (int s = 0; s < C::kSlots && s < issued; ++s) {
+          const int last = s + ((issued - 1 - s) / C::kSlots) * C::kSlots;
+          mbar_wait_drain(&sh.kv_full[s], (last / C::kSlots) & 1, &g_err_fwd);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one() && n_max > 0) {
+      const uint32_t q_addr = smem_u32(s_q);
+      const uint32_t kv_addr = smem_u32(s_kv);
+      auto issue_s = [&](int t, int slot) {
+        const uint32_t a0 = q_addr + t * C::kTileBytes;
+        const uint32_t b0 = kv_addr + slot * C::kTileBytes;
+        for (int kk = 0; kk < C::kQKSteps; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          issue_mma(FP8, tmem + t * kBN, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
+                    C::kIdescS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint32_t b0 = kv_addr + slot * C::kTileBytes;
+        for (int kk = 0; kk < C::kPVSteps; ++kk) {
+          issue_mma_ts(FP8, tmem + 256 + t * D, tmem + t * kBN + kk * 8,
+                       sdesc_sw128(b0 + kk * C::kKPerMma * 128, C::kBlockBytes, 1024), C::kIdescPV,
+                       (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(&sh.q_full, 0, &sh.abort, &g_err_fwd);
+      auto wait_load = [&](int idx) {
+        return mbar_wait(&sh.kv_full[idx % C::kSlots], (idx / C::kSlots) & 1, &sh.abort, &g_err_fwd);
+      };
+      if (ok) ok = wait_load(0);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (n_t[t] > 0) {
+            issue_s(t, 0);
+            tc_commit(&sh.s_full[t]);
+          }
+        tc_commit(&sh.kv_empty[0]);
+      }
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int v_idx = 2 * j + 1;
+        const int k_idx = 2 * j + 2;
+        ok = wait_load(v_idx);
+        const bool has_next = (j + 1 < n_max);
+        bool k_ready = false;
+        for (int t = 0; ok && t < 2; ++t) {
+          if (j < n_t[t]) {
+            ok = mbar_wait(&sh.p_full[t], j & 1, &sh.abort, &g_err_fwd);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, v_idx % C::kSlots, j > 0);
+            tc_commit(&sh.o_done[t]);
+          }
+          if (t == 1) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
+          if (has_next && j + 1 < n_t[t]) {
+            if (!k_ready) {
+              ok = wait_load(k_idx);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            // P_t(j) lives in S_t's columns: S_t(j+1) may only be written
+            // once PV_t(j) has read it.
+            ok = mbar_wait(&sh.o_done[t], j & 1, &sh.abort, &g_err_fwd);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(t, k_idx % C::kSlots);
+            tc_commit(&sh.s_full[t]);
+          }
+        }
+        if (ok && has_next) {
+          if (!k_ready) {  // no tile needed K_{j+1}: cannot happen, kept for safety
+            ok = wait_load(k_idx);
+            tc_fence_after();
+          }
+          tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
+        }
+      }
+      // Teardown: every MMA issued by this thread completes before TMEM is freed.
+      tc_commit(&sh.drain);
+      mbar_wait_drain(&sh.drain, 0, &g_err_fwd);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;              // query tile of this warpgroup
+    const int r = threadIdx.x & 127;      // row within the tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_col = tmem + lane_base + t * kBN;
+    const uint32_t o_col = tmem + lane_base + 256 + t * D;
+    const int row_g = q0 + t * kBM + r;
+    const int nt = n_t[t];
+    float c = scale_log2;
+    float o_mult = 1.0f;
+    if (FP8) {
+      c = scale_log2 * __ldg(descale_q) * __ldg(descale_k);
+      o_mult = __ldg(descale_v) / C::kPScale;
+    }
+    float m_used = -INFINITY;
+    float l_sum = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = mbar_wait(&sh.s_full[t], j & 1, &sh.abort, &g_err_fwd);
+      if (!ok) break;
+      tc_fence_after();
+      float s[kBN];
+      {
+        uint32_t rr[32];
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          tmem_ld32(s_col + cc * 32, rr);
+          tmem_ld_wait(rr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(rr[i]);
+        }
+      }
+      const int key0 = j * kBN;
+      const bool need_mask = (causal && key0 + kBN - 1 > q0 + t * kBM) || (key0 + kBN > N);
+      if (need_mask) {
+        const int lim = causal ? min(row_g, N - 1) : N - 1;  // last visible key
+#pragma unroll
+        for (int i = 0; i < kBN; ++i)
+          if (key0 + i > lim) s[i] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      const float m_cand = mx * c;
+      if (j == 0) {
+        m_used = m_cand;
+      } else {
+        const bool raise = m_cand > m_used + C::kTauLog2;
+        if (__any_sync(0xffffffffu, raise)) {
+          const float alpha = raise ? ex2_approx(m_used - m_cand) : 1.0f;
+          if (raise) m_used = m_cand;
+          l_sum *= alpha;
+          // O_t(j-1) is complete: S_t(j) was issued only after PV_t(j-1) finished.
+#pragma unroll 1
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t rr[32];
+            tmem_ld32(o_col + cc, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(o_col + cc, rr);
+          }
+        }
+      }
+      const float neg_m = -m_used;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < kBN; ++i) {
+        s[i] = ex2_approx(fmaf(s[i], c, neg_m));
+        part[i & 3] += s[i];
+      }
+      l_sum += (part[0] + part[1]) + (part[2] + part[3]);
+      if (FP8) {
+        uint32_t pw[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          pw[i] = pack_e4m3x4(s[4 * i] * C::kPScale, s[4 * i + 1] * C::kPScale, s[4 * i + 2] * C::kPScale,
+                              s[4 * i + 3] * C::kPScale);
+        tmem_st32(s_col, pw);
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pw[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]);
+          tmem_st32(s_col + h * 32, pw);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sh.p_full[t]);
+    }
+    if (ok && nt > 0) {
+      ok = mbar_wait(&sh.o_done[t], (nt - 1) & 1, &sh.abort, &g_err_fwd);
+      tc_fence_after();
+      if (ok) {
+        const float inv = o_mult / l_sum;
+        const bool store = row_g < N;
+        __nv_bfloat16* dst = out_o + (static_cast<size_t>(bh) * N + (store ? row_g : 0)) * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t rr[32];
+          tmem_ld32(o_col + cc, rr);
+          tmem_ld_wait(rr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
+          if (store) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (store) out_lse[static_cast<size_t>(bh) * N + row_g] = m_used * 0.69314718055994531f + logf(l_sum);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool FP8>
+fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D, FP8>;
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv;
+  if (!encode_rows_map(&mq, a.q, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBM) ||
+      !encode_rows_map(&mk, a.k, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBN) ||
+      !encode_rows_map(&mv, a.v, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBN))
+    return FA_ERR_LAUNCH;
+  auto kern = fa_fwd_kernel<D, FP8>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  dim3 grid(static_cast<unsigned>(((a.N + 2 * kBM - 1) / (2 * kBM)) * BH));
+  const float scale_log2 = a.scale * 1.4426950408889634f;
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.descale_q,
+                                                   a.descale_k, a.descale_v, BH, a.N, a.causal, scale_log2);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
+  return a.d == 64 ? launch_fwd_impl<64, false>(a, stream) : launch_fwd_impl<128, false>(a, stream);
+}
+
+fa_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) { return launch_fwd_impl<128, true>(a, stream); }
+
+uint32_t fwd_bf16_take_error(cudaStream_t s) {
+  uint32_t v = 0, zero = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_err_fwd, sizeof(v), 0, cudaMemcpyDeviceToHost, s);
+  cudaStreamSynchronize(s);
+  cudaMemcpyToSymbolAsync(g_err_fwd, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+  cudaStreamSynchronize(s);
+  return v;
+}
+
+uint32_t fwd_fp8_take_error(cudaStream_t) { return 0; }  // shares the word above
+
+}  // namespace fa

@@ -1,0 +1,65 @@
+// Host-side helpers shared by the launchers: TMA tensor-map encoding through
+// the driver entry point, argument structs and the launcher declarations.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Encodes a 3-D tiled map over a [BH, N, cols] row-major tensor of
+// `elem_bytes`-byte elements with a box of (box_cols x box_rows x 1) and the
+// 128-byte swizzle.  Rows past N read as zeros.  Returns false on failure.
+bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, int cols, int N, int BH, int box_cols,
+                     int box_rows);
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const float* descale_q;  // FP8 only (device pointers)
+  const float* descale_k;
+  const float* descale_v;
+  int B, H, N, d;
+  int causal;
+  float scale;
+};
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* lse;
+  const void* dO;
+  const float* D;
+  float* dq_acc;
+  void* dk;
+  void* dv;
+  int B, H, N, d;
+  int causal;
+  float scale;
+};
+
+fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);
+fa_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream);
+fa_status launch_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, long long rows, int d,
+                                cudaStream_t stream);
+fa_status launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
+fa_status launch_bwd_dq_convert(const float* dq_acc, void* dq, long long rows, int d, float scale,
+                                cudaStream_t stream);
+fa_status launch_timeout_probe(unsigned int limit_us, cudaStream_t stream);
+
+// Reads and clears each translation unit's device error word (stream-ordered
+// copy followed by a stream synchronisation done by the caller).
+uint32_t fwd_bf16_take_error(cudaStream_t s);
+uint32_t fwd_fp8_take_error(cudaStream_t s);
+uint32_t bwd_take_error(cudaStream_t s);
+uint32_t probe_take_error(cudaStream_t s);
+
+}  // namespace fa

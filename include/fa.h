@@ -1,0 +1,150 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa_gb300.so).
+ *
+ * The library computes exact scaled-dot-product attention
+ *     S = scale * Q K^T  (S_ij = -inf for j > i when causal),
+ *     P = softmax(S) row by row,  O = P V,
+ * tiled so that S and P never reach device memory, and its gradient.  The
+ * definitions follow "FLASH-ATTN" (taking-lying-flat), FlashAttention-2 >
+ * Background (standard attention and its backward chain) and
+ * FlashAttention-2 > FlashAttention-2 (online softmax with an unscaled output
+ * accumulator, the LogSumExp statistic L = m + log(l), the causal mask and the
+ * skip of fully masked blocks).  The pages write S = QK^T; the softmax scale
+ * is this interface's explicit `scale` argument.
+ *
+ * Common conventions for every entry point
+ *  - Tensors are dense, contiguous, row-major [B, H, N, d] (batch, head,
+ *    sequence, head dimension); the statistics L and D are [B, H, N] fp32.
+ *    Element types: bf16 for Q, K, V, O, dO, dQ, dK, dV; e4m3 bytes for the
+ *    FP8 inputs.
+ *  - All tensor pointers are DEVICE pointers owned by the caller; every
+ *    pointer must be 16-byte aligned.  The library never allocates or frees
+ *    memory, never synchronises the stream (fa_device_error excepted) and
+ *    keeps no state between calls except a once-resolved driver entry point
+ *    and a device error word per kernel family.
+ *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *    default stream.  Launches are asynchronous on that stream.
+ *  - Supported shapes: B, H, N >= 1, d in {64, 128}; B * H <= 2^31 / N.
+ *    Rows past N in the last tile of a head are handled inside the kernels
+ *    (loads past the end read zeros; masked keys get weight 0; nothing is
+ *    stored past row N - 1).
+ *  - scale must be finite and > 0 (usually 1/sqrt(d)).
+ *  - Return value: FA_OK, or the first argument / launch error found; on an
+ *    error nothing has been launched by that call, except FA_ERR_LAUNCH which
+ *    reports a failed launch.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, B/H/N <= 0, bad scale, size overflow */
+  FA_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, or no sm_103 device current    */
+  FA_ERR_ALIGNMENT = 3,   /* a tensor pointer not 16-byte aligned                */
+  FA_ERR_LAUNCH = 4,      /* a kernel launch or tensor-map encoding failed       */
+  FA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (fa_device_error)   */
+  FA_ERR_WORKSPACE = 6    /* workspace missing or smaller than required          */
+} fa_status;
+
+/*
+ * Forward pass ("FLASH-ATTN", FlashAttention-2 > FlashAttention-2).
+ *   q, k, v : [B,H,N,d] bf16, read only.
+ *   o       : [B,H,N,d] bf16, written: O = softmax(scale*QK^T [+mask]) V.
+ *   lse     : [B,H,N] fp32, written: L_i = ln sum_j exp(scale * q_i.k_j) over
+ *             the unmasked keys (natural-log units of the scaled logits).
+ *   causal  : 0 or 1 (mask S_ij = -inf for j > i, self-attention).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 int causal, float scale, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: D ([B,H,N] fp32, 16-byte padded)
+ * followed by the fp32 dQ accumulator ([B,H,N,d]).  0 on invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass ("FLASH-ATTN", FlashAttention-2 > Background: dV = P^T dO,
+ * dP = dO V^T, dS = dsoftmax(dP), dQ = dS K, dK = dS^T Q; P rebuilt from L as
+ * in FlashAttention > Tiling and Recomputation).  With S = scale*QK^T the
+ * gradients w.r.t. Q and K carry the factor `scale`.
+ *   q, k, v, o, dO : [B,H,N,d] bf16 read only (o and lse from fa_fwd with the
+ *                    same q, k, v, causal, scale).
+ *   lse            : [B,H,N] fp32 read only.
+ *   dq, dk, dv     : [B,H,N,d] bf16 written.
+ *   workspace      : device buffer of at least fa_bwd_workspace_size() bytes;
+ *                    contents on entry do not matter; overwritten.
+ * Runs fa_bwd_preprocess, fa_bwd_main and fa_bwd_dq_convert on `stream`.
+ * dQ is reduced with fp32 atomics, so its low bits may vary run to run.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 int causal, float scale, void* stream);
+
+/*
+ * Backward step 1: D_i = sum_k dO_ik O_ik (fp32), which equals
+ * sum_j P_ij dP_ij, the row term of the softmax Jacobian; also zeroes dq_acc.
+ *   o, dO  : [B,H,N,d] bf16.  D: [B,H,N] fp32 out.  dq_acc: [B,H,N,d] fp32 out (zeros).
+ */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, int B, int H, int N, int d,
+                            void* stream);
+
+/*
+ * Backward step 2: one CTA per 128-key block of a head, Q blocks inner
+ * ("FLASH-ATTN", FlashAttention-2 > Parallelism: the backward pass gives each
+ * column block its own thread block and the blocks meet only in atomic adds
+ * to dQ).  Writes dK = scale * dS^T Q and dV = P^T dO (bf16) and adds
+ * dS K (unscaled, fp32) into dq_acc, which must hold zeros on entry (step 1).
+ */
+fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* lse, const void* dO,
+                      const float* D, float* dq_acc, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                      float scale, void* stream);
+
+/* Backward step 3: dq = bf16(scale * dq_acc), round to nearest even. */
+fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d, float scale, void* stream);
+
+/*
+ * FP8 forward ("FLASH-ATTN", FlashAttention-3 > Low-precision with FP8:
+ * per-tensor scaling keeps one scalar per tensor).
+ *   q8, k8, v8 : [B,H,N,d] e4m3 codes (1 byte each); X = delta_X * code.
+ *   descale_q, descale_k, descale_v : DEVICE pointers to one fp32 each (delta).
+ *   o   : [B,H,N,d] bf16 out, O = softmax(scale * (dq dk) q8 k8^T) (dv v8).
+ *   lse : [B,H,N] fp32 out, natural-log LogSumExp of the scaled logits.
+ * Inside, P is stored as e4m3 times 2^8 for the second product; the factor is
+ * removed in the final division by the row sum.
+ */
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale_q,
+                     const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H, int N,
+                     int d, int causal, float scale, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error words of all
+ * kernel families.  FA_ERR_TIMEOUT if any kernel recorded a wait that ran out
+ * since the last call; FA_ERR_LAUNCH if the stream reports a CUDA error;
+ * FA_OK otherwise.
+ */
+fa_status fa_device_error(void* stream);
+
+/*
+ * Test hook for the timeout path: launches one CTA whose thread waits on an
+ * mbarrier that nothing ever completes, with a limit of about `limit_us`
+ * microseconds (1..1000000); the kernel records a timeout and returns.  A
+ * following fa_device_error() must report FA_ERR_TIMEOUT.
+ */
+fa_status fa_debug_wait_timeout(unsigned int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI: the library builds, loads and exports every
+symbol include/fa.h declares; argument checks that return before any device
+work.  No compute call is made here (this runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_76_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_expected_entry_points():
+    syms = declared_symbols()
+    for name in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_fp8", "fa_status_string",
+                 "fa_device_error", "fa_bwd_preprocess", "fa_bwd_main", "fa_bwd_dq_convert"):
+        assert name in syms
+    assert set(syms) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(_lib.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.fa_status_string(code).decode()
+        assert s.startswith(_lib.STATUS_NAMES[code])
+
+
+def test_workspace_size(lib):
+    B, H, N, d = 2, 3, 130, 64
+    rows = B * H * N
+    expect = ((rows * 4 + 15) // 16) * 16 + rows * d * 4
+    assert lib.fa_bwd_workspace_size(B, H, N, d) == expect
+    assert lib.fa_bwd_workspace_size(1, 1, 1, 96) == 0
+    assert lib.fa_bwd_workspace_size(0, 1, 1, 64) == 0
+
+
+ALIGNED = 0x10000
+
+
+def fwd(lib, q=ALIGNED, k=ALIGNED, v=ALIGNED, o=ALIGNED, lse=ALIGNED, B=1, H=1, N=128, d=64, causal=0,
+        scale=0.125):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, None)
+
+
+def test_fwd_argument_errors_before_any_launch(lib):
+    assert fwd(lib, q=None) == 1
+    assert fwd(lib, lse=None) == 1
+    assert fwd(lib, k=ALIGNED + 8) == 3
+    assert fwd(lib, N=0) == 1
+    assert fwd(lib, B=-1) == 1
+    assert fwd(lib, d=96) == 2
+    assert fwd(lib, d=256) == 2
+    assert fwd(lib, scale=float("nan")) == 1
+    assert fwd(lib, scale=0.0) == 1
+    assert fwd(lib, scale=-1.0) == 1
+    assert fwd(lib, causal=2) == 1
+
+
+def test_bwd_argument_errors_before_any_launch(lib):
+    p = ALIGNED
+    args = [p] * 10 + [10 ** 9, 1, 1, 128, 64, 0, 0.125, None]
+    assert lib.fa_bwd(*args[:9], None, *args[10:]) == 6      # no workspace
+    small = list(args); small[10] = 16
+    assert lib.fa_bwd(*small) == 6                            # too small
+    mis = list(args); mis[9] = p + 4
+    assert lib.fa_bwd(*mis) == 3                              # misaligned workspace
+    nul = list(args); nul[6] = None
+    assert lib.fa_bwd(*nul) == 1
+
+
+def test_fp8_argument_errors_before_any_launch(lib):
+    p = ALIGNED
+    assert lib.fa_fwd_fp8(p, p, p, None, p, p, p, p, 1, 1, 128, 128, 0, 0.1, None) == 1
+    assert lib.fa_fwd_fp8(p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0, 0.1, None) == 2
+    assert lib.fa_fwd_fp8(p, p, p + 1, p, p, p, p, p, 1, 1, 128, 128, 0, 0.1, None) == 3
+
+
+def test_debug_timeout_hook_rejects_bad_limit(lib):
+    assert lib.fa_debug_wait_timeout(0, None) == 1
+    assert lib.fa_debug_wait_timeout(2_000_000, None) == 1
+
+
+def test_product_has_no_oracle_import():
+    pkg = os.path.join(ROOT, "exact_attention_76_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
