@@ -30,6 +30,7 @@ SIGNATURES = {
     "fa_status_string": ([_I], ctypes.c_char_p),
     "fa_device_error": ([_P], _I),
     "fa_debug_wait_timeout": ([_U, _P], _I),
+    "fa_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
 }
 
 _lib = None

@@ -124,6 +124,26 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
                      const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H, int N,
                      int d, int causal, float scale, void* stream);
 
+/*
+ * fa_bwd without a workspace argument, for callers that cannot allocate
+ * device memory: a plugin inside another runtime that is handed only its
+ * input and output tensors, or code on a path where cudaMalloc (which can
+ * synchronise the device and can fail under memory pressure) is not allowed.
+ * The pages have no counterpart to this entry point.
+ *   Arguments, layouts and results are those of fa_bwd.
+ *   Scratch: a 32 MiB array in the library's own device memory (present on
+ *   every GPU that loads the library until the process exits).  Sizes whose
+ *   fa_bwd_workspace_size() exceeds 32 MiB return FA_ERR_WORKSPACE before any
+ *   launch.  All calls share the array; each call re-initialises what it
+ *   reads, but calls that overlap on the GPU race, so order them on one
+ *   stream.  The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current): make it before any
+ *   stream capture.  Allocates nothing.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+                         float scale, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* fa_status_string(fa_status s);
 
