@@ -35,6 +35,8 @@
 //  warp 9     TMEM allocation and the single MMA-issuing thread.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "fa_common.cuh"
 #include "fa_host.h"
 
@@ -103,16 +105,19 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __r
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;   // one 128-row bf16 tile
-  static constexpr int kColBlocks = D / 64;        // 128-byte column blocks per row
-  static constexpr int kBlockBytes = 128 * 128;
-  static constexpr int kDsBytes = 128 * 128 * 2;   // dS^T, 128 keys x 128 queries
+  static constexpr int kColBlocks = D / 64;        // 128-byte column blocks per bf16 row
+  static constexpr int kBlockBytes = 128 * 128;    // one 128-row x 128-byte block
+  static constexpr int kDsBytes = 128 * 128 * 2;   // dS^T, 128 keys x 128 queries, bf16
+  static constexpr int kStageBytes = 32768;        // dQ staging: 2 blocks of 128 rows x 32 fp32
+  static constexpr int kDqRounds = (D * 4) / 256;  // dQ row = D fp32; 64 columns (2 blocks) per round
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffQ = kOffV + kTileBytes;           // 2 stages
-  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;      // 2 stages
-  static constexpr int kOffDS = kOffDO + 2 * kTileBytes;
-  static constexpr int kOffL = kOffDS + kDsBytes;            // float [2][128]
+  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;      // 1 stage
+  static constexpr int kOffDS = kOffDO + kTileBytes;
+  static constexpr int kOffStage = kOffDS + kDsBytes;
+  static constexpr int kOffL = kOffStage + kStageBytes;      // float [2][128]
   static constexpr int kOffDv = kOffL + 2 * 128 * 4;         // float [2][128]
   static constexpr int kOffBar = kOffDv + 2 * 128 * 4;
   static constexpr int kSmemBytes = kOffBar + 256;
@@ -125,26 +130,41 @@ struct BwdCfg {
   static constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t kIdescKM = idesc_bf16(128, D, false, true);
   static constexpr uint32_t kIdescMM = idesc_bf16(128, D, true, true);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t qdo_full[2];
-  uint64_t qdo_empty[2];
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t do_full, do_empty;
   uint64_t ld_full[2];
   uint64_t ld_empty[2];
-  uint64_t s_full, p_ready, dp_full, ds_ready, dv_done, ds_free, dq_full, dq_free, acc_done, drain;
+  uint64_t s_full, p_ready, dp_full, ds_ready, dv_done, dq_full, dq_free, acc_done, drain;
   uint32_t tmem_base;
   CtaAbort abort;
 };
+
+// Block index -> (head, key block).  Heads are taken in groups whose Q, dO
+// and dQ accumulator fit in L2 together; within a group the key blocks with
+// the most query blocks (causal: the lowest) come first.
+__device__ __forceinline__ void bwd_item(int item, int BH, int n_blk, int group, int& bh, int& kb) {
+  const int per_group = group * n_blk;
+  const int g = item / per_group;
+  const int r = item - g * per_group;
+  const int g_heads = min(group, BH - g * group);
+  kb = r / g_heads;
+  bh = g * group + (r - kb * g_heads);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                       const float* __restrict__ lse, const float* __restrict__ dvec, float* __restrict__ dq_acc,
-                       __nv_bfloat16* __restrict__ dk_out, __nv_bfloat16* __restrict__ dv_out, int BH, int N,
-                       int causal, float scale, float scale_log2) {
+                       const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse,
+                       const float* __restrict__ dvec, __nv_bfloat16* __restrict__ dk_out,
+                       __nv_bfloat16* __restrict__ dv_out, int BH, int N, int causal, float scale,
+                       float scale_log2, int head_group) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   static_assert(sizeof(BwdBars) <= 256, "barrier block");
@@ -162,9 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id();
   const int n_blk = (N + 127) / 128;
-  const int item = static_cast<int>(blockIdx.x);
-  const int kb = item / BH;  // key block; ascending = most work first under a causal mask
-  const int bh = item % BH;
+  int bh, kb;
+  bwd_item(static_cast<int>(blockIdx.x), BH, n_blk, head_group, bh, kb);
   const int i_begin = causal ? kb : 0;
   const int n_it = n_blk - i_begin;
 
@@ -172,17 +191,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.abort.flag = 0;
     mbar_init(&sh.kv_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sh.qdo_full[s], 1);
-      mbar_init(&sh.qdo_empty[s], 1);
+      mbar_init(&sh.q_full[s], 1);
+      mbar_init(&sh.q_empty[s], 1);
       mbar_init(&sh.ld_full[s], 32);
       mbar_init(&sh.ld_empty[s], 128);
     }
+    mbar_init(&sh.do_full, 1);
+    mbar_init(&sh.do_empty, 1);
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.p_ready, 128);
     mbar_init(&sh.dp_full, 1);
     mbar_init(&sh.ds_ready, 128);
     mbar_init(&sh.dv_done, 1);
-    mbar_init(&sh.ds_free, 1);
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_free, 128);
     mbar_init(&sh.acc_done, 1);
@@ -207,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + C::kOffV + cb * C::kBlockBytes, &map_v, cb * 64, kb * 128, bh, &sh.kv_full);
       }
     }
-    int issued[2] = {0, 0};  // Q/dO loads issued per stage (lane 0)
+    int q_issued[2] = {0, 0};
+    int do_issued = 0;
     for (int it = 0; it < n_it; ++it) {
       if (__shfl_sync(0xffffffffu, sh.abort.flag, 0)) break;  // one decision for the whole warp
       const int st = it & 1;
@@ -215,16 +236,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qrow0 = (i_begin + it) * 128;
       bool ok = true;
       if (lane == 0) {
-        if (use > 0) ok = mbar_wait(&sh.qdo_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd);
+        // Q_i: two stages, freed when dK_(i-2) has read it.
+        if (use > 0) ok = mbar_wait(&sh.q_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd);
         if (ok) {
-          mbar_arrive_expect_tx(&sh.qdo_full[st], 2 * C::kTileBytes);
-          for (int cb = 0; cb < C::kColBlocks; ++cb) {
+          mbar_arrive_expect_tx(&sh.q_full[st], C::kTileBytes);
+          for (int cb = 0; cb < C::kColBlocks; ++cb)
             tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * 64, qrow0, bh,
-                        &sh.qdo_full[st]);
-            tma_load_3d(smem + C::kOffDO + st * C::kTileBytes + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, bh,
-                        &sh.qdo_full[st]);
-          }
-          ++issued[st];
+                        &sh.q_full[st]);
+          ++q_issued[st];
+        }
+        // dO_i: one stage, freed when dV_(i-1) has read it.
+        if (ok && it > 0) ok = mbar_wait(&sh.do_empty, (it - 1) & 1, &sh.abort, &g_err_bwd);
+        if (ok) {
+          mbar_arrive_expect_tx(&sh.do_full, C::kTileBytes);
+          for (int cb = 0; cb < C::kColBlocks; ++cb)
+            tma_load_3d(smem + C::kOffDO + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, bh, &sh.do_full);
+          ++do_issued;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -249,43 +276,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Let every copy still in flight land before the CTA's memory goes away.
       mbar_wait_drain(&sh.kv_full, 0, &g_err_bwd);
       for (int s2 = 0; s2 < 2; ++s2)
-        if (issued[s2] > 0) mbar_wait_drain(&sh.qdo_full[s2], (issued[s2] - 1) & 1, &g_err_bwd);
+        if (q_issued[s2] > 0) mbar_wait_drain(&sh.q_full[s2], (q_issued[s2] - 1) & 1, &g_err_bwd);
+      if (do_issued > 0) mbar_wait_drain(&sh.do_full, (do_issued - 1) & 1, &g_err_bwd);
     }
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Per query block i the five products are issued as
+    //   dV_i, S_(i+1), dK_i, dQ_i, dP_(i+1)
+    // so the key-row warpgroup computes P_(i+1) while dK_i and dQ_i run.
     if (elect_one()) {
       const uint32_t sm = smem_u32(smem);
       const uint32_t k_addr = sm + C::kOffK, v_addr = sm + C::kOffV, ds_addr = sm + C::kOffDS;
-      bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_err_bwd);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int st = it & 1;
-        const uint32_t q_addr = sm + C::kOffQ + st * C::kTileBytes;
-        const uint32_t do_addr = sm + C::kOffDO + st * C::kTileBytes;
-        ok = mbar_wait(&sh.qdo_full[st], (it >> 1) & 1, &sh.abort, &g_err_bwd);
-        if (ok && it > 0) ok = mbar_wait(&sh.dv_done, (it - 1) & 1, &sh.abort, &g_err_bwd);  // P^T read
-        if (!ok) break;
-        tc_fence_after();
-        // S^T = K Q_i^T
+      const uint32_t do_addr = sm + C::kOffDO;
+      auto issue_s = [&](int i) {  // S^T = K Q_i^T
+        const uint32_t q_addr = sm + C::kOffQ + (i & 1) * C::kTileBytes;
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
           mma_bf16_ss(tmem + C::kTmS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
                       C::kIdescKK, kk > 0);
         }
         tc_commit(&sh.s_full);
-        if (D == 128 && it > 0) {  // dP^T shares columns with dQ_(i-1)
-          ok = mbar_wait(&sh.dq_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        // dP^T = V dO_i^T
+      };
+      auto issue_dp = [&]() {  // dP^T = V dO_i^T
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
           mma_bf16_ss(tmem + C::kTmDP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
                       C::kIdescKK, kk > 0);
         }
         tc_commit(&sh.dp_full);
-        // dV += P^T dO_i
+      };
+      bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_err_bwd) &&
+                mbar_wait(&sh.q_full[0], 0, &sh.abort, &g_err_bwd);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = mbar_wait(&sh.do_full, 0, &sh.abort, &g_err_bwd);
+        if (ok) {
+          tc_fence_after();
+          issue_dp();
+        }
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it & 1;
+        const uint32_t q_addr = sm + C::kOffQ + st * C::kTileBytes;
+        const bool has_next = it + 1 < n_it;
+        // dV += P_i^T dO_i
         ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
         if (!ok) break;
         tc_fence_after();
@@ -293,7 +329,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmS + kk * 8, sdesc_sw128(do_addr + kk * 2048, C::kBlockBytes, 1024),
                       C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sh.dv_done);
-        // dK += dS^T Q_i ; dQ_i = dS K
+        tc_commit(&sh.do_empty);
+        // S_(i+1): its columns hold P_i^T until dV_i has read them.
+        if (has_next) {
+          ok = mbar_wait(&sh.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, &sh.abort, &g_err_bwd) &&
+               mbar_wait(&sh.dv_done, it & 1, &sh.abort, &g_err_bwd);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(it + 1);
+        }
+        // dK += dS_i^T Q_i ; dQ_i = dS_i K
         ok = mbar_wait(&sh.ds_ready, it & 1, &sh.abort, &g_err_bwd);
         if (!ok) break;
         tc_fence_after();
@@ -302,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + C::kTmDK, sdesc_sw128(ds_addr + off, 16, 1024),
                       sdesc_sw128(q_addr + kk * 2048, C::kBlockBytes, 1024), C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
         }
+        tc_commit(&sh.q_empty[st]);
         if (D == 64 && it > 0) {  // separate dQ columns: only the previous read-out must be done
           ok = mbar_wait(&sh.dq_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
           if (!ok) break;
@@ -311,8 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + C::kTmDQ, sdesc_sw128(ds_addr + kk * 2048, C::kBlockBytes, 1024),
                       sdesc_sw128(k_addr + kk * 2048, C::kBlockBytes, 1024), C::kIdescMM, kk > 0);
         tc_commit(&sh.dq_full);
-        tc_commit(&sh.ds_free);
-        tc_commit(&sh.qdo_empty[st]);
+        // dP_(i+1)
+        if (has_next) {
+          ok = mbar_wait(&sh.do_full, (it + 1) & 1, &sh.abort, &g_err_bwd);
+          if (ok && D == 128)  // dP^T shares columns with dQ_i
+            ok = mbar_wait(&sh.dq_free, it & 1, &sh.abort, &g_err_bwd);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp();
+        }
       }
       if (ok) tc_commit(&sh.acc_done);
       tc_commit(&sh.drain);
@@ -360,8 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sh.p_ready);
+      // dS_i may overwrite dS_(i-1) once dK_(i-1) and dQ_(i-1) have read it.
       ok = mbar_wait(&sh.dp_full, it & 1, &sh.abort, &g_err_bwd);
-      if (ok && it > 0) ok = mbar_wait(&sh.ds_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
+      if (ok && it > 0) ok = mbar_wait(&sh.dq_full, (it - 1) & 1, &sh.abort, &g_err_bwd);
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
@@ -369,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rr[32];
         tmem_ld32(tmem + lane_base + C::kTmDP + cc * 32, rr);
         tmem_ld_wait(rr);
-        // 32 queries = two 16-byte chunks of 8 in column block cc/2
+        // 32 queries = four 16-byte chunks of 8 in column block cc/2
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -386,8 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
         }
       }
-      // generic-proxy stores -> visible to the tensor core's async proxy
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      fence_proxy_async_smem();  // generic-proxy stores -> tensor core reads
       tc_fence_before();
       mbar_arrive(&sh.ds_ready);
       mbar_arrive(&sh.ld_empty[st]);
@@ -413,10 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ dQ read-out (query rows), dK epilogue
+    // ------------------------------------------------------------ dQ reduction (query rows), dK epilogue
+    // dQ_i goes TMEM -> registers -> swizzled staging in shared memory ->
+    // TMA reduce-add into the fp32 accumulator (the tensor map clips rows past N).
     const int r = threadIdx.x - 128;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+    uint8_t* stage_row = smem + C::kOffStage + r * 128;
+    const bool leader = (threadIdx.x == 128);
     bool ok = true;
+    bool staged_before = false;
     for (int it = 0; it < n_it; ++it) {
       ok = mbar_wait(&sh.dq_full, it & 1, &sh.abort, &g_err_bwd);
       if (!ok) break;
@@ -432,14 +491,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&sh.dq_free);
-      const int qg = (i_begin + it) * 128 + r;
-      if (qg < N) {
-        float4* dst = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * N + qg) * D);
+      const int qrow0 = (i_begin + it) * 128;
 #pragma unroll
-        for (int i = 0; i < D / 4; ++i)
-          atomicAdd(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+      for (int round = 0; round < C::kDqRounds; ++round) {
+        if (staged_before) {
+          if (leader) bulk_wait_read_all();  // the previous reduce has read the staging buffer
+          named_bar_sync(1, 128);
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {  // two 32-column blocks of 128 rows x 128 bytes
+          uint8_t* blk = stage_row + b * C::kBlockBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int col = round * 64 + b * 32 + c * 4;
+            *reinterpret_cast<float4*>(blk + ((static_cast<uint32_t>(c) ^ swz) << 4)) =
+                make_float4(v[col], v[col + 1], v[col + 2], v[col + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader) {
+          tma_reduce_add_3d(&map_dq, round * 64, qrow0, bh, smem + C::kOffStage);
+          tma_reduce_add_3d(&map_dq, round * 64 + 32, qrow0, bh, smem + C::kOffStage + C::kBlockBytes);
+          bulk_commit_group();
+        }
+        staged_before = true;
       }
     }
+    if (leader) bulk_wait_all();
     // dK = scale * sum_i dS_i^T Q_i
     if (ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd)) {
       tc_fence_after();
@@ -476,18 +555,24 @@ template <int D>
 fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const int BH = a.B * a.H;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!encode_rows_map(&mq, a.q, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mk, a.k, 2, D, a.N, BH, 64, 128) ||
-      !encode_rows_map(&mv, a.v, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdo, a.dO, 2, D, a.N, BH, 64, 128))
+      !encode_rows_map(&mv, a.v, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdo, a.dO, 2, D, a.N, BH, 64, 128) ||
+      !encode_rows_map(&mdq, a.dq_acc, 4, D, a.N, BH, 32, 128))
     return FA_ERR_LAUNCH;
   auto kern = fa_bwd_main_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FA_ERR_LAUNCH;
   const int n_blk = (a.N + 127) / 128;
+  // Heads per group: Q, dO (bf16) and the dQ accumulator (fp32) of a group
+  // should stay within about 48 MB of the L2.
+  const long long head_bytes = static_cast<long long>(a.N) * D * (2 + 2 + 4);
+  int group = static_cast<int>(std::max<long long>(1, (48ll << 20) / head_bytes));
+  group = std::min(group, BH);
   dim3 grid(static_cast<unsigned>(n_blk * BH));
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, a.lse, a.D, a.dq_acc,
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a.lse, a.D,
                                                    static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv),
-                                                   BH, a.N, a.causal, a.scale, a.scale * kLog2e);
+                                                   BH, a.N, a.causal, a.scale, a.scale * kLog2e, group);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
