@@ -396,11 +396,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + C::kTmS + cc * 32, rr);
         tmem_ld_wait(rr);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int q = cc * 32 + i;
-          float x = ex2_approx(fmaf(__uint_as_float(rr[i]), scale_log2, -l2[q]));
-          if (diag && q < r) x = 0.f;  // query before key: masked
-          p[q] = x;
+        for (int i4 = 0; i4 < 8; ++i4) {  // L for 4 queries per 16-byte broadcast load
+          const float4 lq = reinterpret_cast<const float4*>(l2)[cc * 8 + i4];
+          const float lv[4] = {lq.x, lq.y, lq.z, lq.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i4 * 4 + u;
+            const int q = cc * 32 + i;
+            float x = ex2_approx(fmaf(__uint_as_float(rr[i]), scale_log2, -lv[u]));
+            if (diag && q < r) x = 0.f;  // query before key: masked
+            p[q] = x;
+          }
         }
       }
 #pragma unroll
@@ -426,11 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 32 queries = four 16-byte chunks of 8 in column block cc/2
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int q0 = cc * 32 + 2 * i;
-          const float a = p[q0] * (__uint_as_float(rr[2 * i]) - dd[q0]);
-          const float b = p[q0 + 1] * (__uint_as_float(rr[2 * i + 1]) - dd[q0 + 1]);
-          w[i] = pack_bf16x2(a, b);
+        for (int i2 = 0; i2 < 8; ++i2) {  // D for 4 queries per 16-byte broadcast load
+          const float4 dq4 = reinterpret_cast<const float4*>(dd)[cc * 8 + i2];
+          const int q0 = cc * 32 + 4 * i2;
+          w[2 * i2] = pack_bf16x2(p[q0] * (__uint_as_float(rr[4 * i2]) - dq4.x),
+                                  p[q0 + 1] * (__uint_as_float(rr[4 * i2 + 1]) - dq4.y));
+          w[2 * i2 + 1] = pack_bf16x2(p[q0 + 2] * (__uint_as_float(rr[4 * i2 + 2]) - dq4.z),
+                                      p[q0 + 3] * (__uint_as_float(rr[4 * i2 + 3]) - dq4.w));
         }
         uint8_t* blk = ds_row + (cc >> 1) * C::kBlockBytes;
 #pragma unroll

@@ -79,6 +79,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended
+// (up to `suspend_ns`) until the phase completes, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Per-CTA cancellation state shared by all roles of a kernel.
 struct CtaAbort {
   volatile int flag;
@@ -87,11 +101,14 @@ struct CtaAbort {
 // Waits for the phase with the given parity.  Returns false when the CTA is
 // being aborted or when this wait itself ran out (then it records the timeout
 // in *err and raises the abort flag).
+// kSuspend: each retry suspends the thread (up to 20 us) until the phase
+// completes, which frees issue slots for the other warps of the SM partition.
+template <bool kSuspend = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, CtaAbort* ab, uint32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (kSuspend ? mbar_try_wait_suspend(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
     if (ab->flag) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       atomicOr(err, FA_DEVERR_TIMEOUT);

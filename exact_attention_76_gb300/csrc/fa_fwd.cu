@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
           const int slot = issued % C::kSlots;
           const int round = issued / C::kSlots;
-          if (round > 0 && !mbar_wait(&sh.kv_empty[slot], (round - 1) & 1, &sh.abort, &g_err_fwd)) break;
+          if (round > 0 && !mbar_wait<true>(&sh.kv_empty[slot], (round - 1) & 1, &sh.abort, &g_err_fwd)) break;
           mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
           const CUtensorMap* m = kv == 0 ? &map_k : &map_v;
           for (int cb = 0; cb < C::kColBlocks; ++cb)
@@ -200,9 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(&sh.q_full, 0, &sh.abort, &g_err_fwd);
+      bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd);
       auto wait_load = [&](int idx) {
-        return mbar_wait(&sh.kv_full[idx % C::kSlots], (idx / C::kSlots) & 1, &sh.abort, &g_err_fwd);
+        return mbar_wait<true>(&sh.kv_full[idx % C::kSlots], (idx / C::kSlots) & 1, &sh.abort, &g_err_fwd);
       };
       if (ok) ok = wait_load(0);
       if (ok) {
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool k_ready = false;
         for (int t = 0; ok && t < 2; ++t) {
           if (j < n_t[t]) {
-            ok = mbar_wait(&sh.p_full[t], j & 1, &sh.abort, &g_err_fwd);
+            ok = mbar_wait<true>(&sh.p_full[t], j & 1, &sh.abort, &g_err_fwd);
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, v_idx % C::kSlots, j > 0);
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // P_t(j) lives in S_t's columns: S_t(j+1) may only be written
             // once PV_t(j) has read it.
-            ok = mbar_wait(&sh.o_done[t], j & 1, &sh.abort, &g_err_fwd);
+            ok = mbar_wait<true>(&sh.o_done[t], j & 1, &sh.abort, &g_err_fwd);
             if (!ok) break;
             tc_fence_after();
             issue_s(t, k_idx % C::kSlots);
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_sum = 0.0f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = mbar_wait(&sh.s_full[t], j & 1, &sh.abort, &g_err_fwd);
+      ok = mbar_wait<true>(&sh.s_full[t], j & 1, &sh.abort, &g_err_fwd);
       if (!ok) break;
       tc_fence_after();
       float s[kBN];
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sh.p_full[t]);
     }
     if (ok && nt > 0) {
-      ok = mbar_wait(&sh.o_done[t], (nt - 1) & 1, &sh.abort, &g_err_fwd);
+      ok = mbar_wait<true>(&sh.o_done[t], (nt - 1) & 1, &sh.abort, &g_err_fwd);
       tc_fence_after();
       if (ok) {
         const float inv = o_mult / l_sum;
