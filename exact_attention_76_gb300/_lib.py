@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3:
 
 # (name, argtypes, restype) for every symbol include/fa.h declares.
 _P, _I, _F, _Z, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint
+_L = ctypes.c_longlong
 SIGNATURES = {
     "fa_fwd": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
     "fa_bwd_workspace_size": ([_I, _I, _I, _I], _Z),
@@ -30,6 +31,7 @@ SIGNATURES = {
     "fa_status_string": ([_I], ctypes.c_char_p),
     "fa_device_error": ([_P], _I),
     "fa_debug_wait_timeout": ([_U, _P], _I),
+    "fa_fp8_quantize": ([_P, _I, _I, _P, _P, _L, _I, _P], _I),
     "fa_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
 }
 

@@ -135,6 +135,27 @@ def fa_fwd_fp8(q8, k8, v8, descale_q, descale_k, descale_v, causal: bool, scale:
     return o, lse
 
 
+def fa_fp8_quantize(x, hadamard: bool, codes=None, descale=None, stream=None):
+    """Per-tensor e4m3 codes of x (optionally rotated by the normalised Hadamard
+    transform along the last dimension) and the fp32 descale.  x: CUDA fp32 or
+    bf16, last dimension 64 or 128.  Returns (codes uint8 of x's shape, descale
+    as a 1-element fp32 tensor)."""
+    lib = _lib.load()
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x: expected fp32 or bf16")
+    _check(x, "x", x.dtype)
+    d = x.shape[-1]
+    rows = x.numel() // d
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if codes is None else codes
+    descale = torch.empty(1, dtype=torch.float32, device=x.device) if descale is None else descale
+    _check(codes, "codes", torch.uint8, tuple(x.shape))
+    _check(descale, "descale", torch.float32)
+    _lib.check("fa_fp8_quantize", lib.fa_fp8_quantize(_ptr(x), 1 if x.dtype == torch.bfloat16 else 0,
+                                                      int(bool(hadamard)), _ptr(codes), _ptr(descale), rows, d,
+                                                      _stream_ptr(stream)))
+    return codes, descale
+
+
 def fa_status_string(status: int) -> str:
     return _lib.load().fa_status_string(int(status)).decode()
 

@@ -218,6 +218,17 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
   return launch_fwd_fp8(a, static_cast<cudaStream_t>(stream));
 }
 
+fa_status fa_fp8_quantize(const void* x, int x_dtype, int hadamard, void* codes, float* descale, long long rows,
+                          int d, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(x, codes, descale)) != FA_OK) return st;
+  if (rows <= 0 || rows > (1LL << 31) || (x_dtype != 0 && x_dtype != 1) || (hadamard != 0 && hadamard != 1))
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((st = check_device()) != FA_OK) return st;
+  return launch_fp8_quantize(x, x_dtype, hadamard, codes, descale, rows, d, static_cast<cudaStream_t>(stream));
+}
+
 const char* fa_status_string(fa_status s) {
   switch (s) {
     case FA_OK: return "FA_OK";

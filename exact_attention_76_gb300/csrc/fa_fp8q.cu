@@ -1,0 +1,136 @@
+// Per-tensor e4m3 storage for the FP8 forward, with optional incoherent
+// processing ("FLASH-ATTN", FlashAttention-3 > Low-precision with FP8: one
+// scale per tensor; Q and K multiplied by an orthogonal matrix M before
+// quantisation, which leaves (QM)(KM)^T = QK^T and spreads outliers;
+// "FlashAttention 三代演进", 技术 4: M is a Hadamard transform).
+//
+//   y      = x H / sqrt(d)     (if rotating; H the Sylvester Hadamard matrix)
+//   delta  = max |y| / 448     (one fp32 per tensor, 448 = largest e4m3)
+//   code   = e4m3_rne(y / delta)
+//
+// One warp per row of d values (d / 32 per lane).  The rotation is a fast
+// Walsh-Hadamard transform: butterflies (a, b) -> (a + b, a - b) over the
+// index bits, first the bits inside a lane's registers, then the lane bits
+// through warp shuffles.  Three launches: max |y| (atomic max on the float's
+// bit pattern, valid for non-negative floats), the codes, and delta.
+#include <cuda_bf16.h>
+
+#include "fa_common.cuh"
+#include "fa_host.h"
+
+namespace fa {
+
+namespace {
+
+template <int D, typename T>
+__device__ __forceinline__ void load_row_rotated(const T* __restrict__ x, long long row, bool rotate,
+                                                 float (&v)[D / 32]) {
+  constexpr int E = D / 32;
+  const int lane = static_cast<int>(lane_id());
+  const T* src = x + row * D + lane * E;
+#pragma unroll
+  for (int j = 0; j < E; ++j) {
+    if constexpr (sizeof(T) == 2) v[j] = __bfloat162float(src[j]);
+    else v[j] = static_cast<float>(src[j]);
+  }
+  if (!rotate) return;
+  // index bits inside the lane: e = lane * E + j
+#pragma unroll
+  for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      if ((j & h) == 0) {
+        const float a = v[j], b = v[j + h];
+        v[j] = a + b;
+        v[j + h] = a - b;
+      }
+    }
+  }
+  // index bits across lanes: partner element is e ^ (m * E), i.e. lane ^ m
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool high = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const float p = __shfl_xor_sync(0xffffffffu, v[j], m);
+      v[j] = high ? (p - v[j]) : (v[j] + p);
+    }
+  }
+  const float norm = rsqrtf(static_cast<float>(D));
+#pragma unroll
+  for (int j = 0; j < E; ++j) v[j] *= norm;
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(256) fp8q_amax_kernel(const T* __restrict__ x, long long rows, int rotate,
+                                                        unsigned int* __restrict__ amax_bits) {
+  const long long warps = static_cast<long long>(gridDim.x) * 8;
+  float m = 0.f;
+  for (long long row = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row < rows; row += warps) {
+    float v[D / 32];
+    load_row_rotated<D>(x, row, rotate != 0, v);
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) m = fmaxf(m, fabsf(v[j]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane_id() == 0) atomicMax(amax_bits, __float_as_uint(m));
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(256) fp8q_codes_kernel(const T* __restrict__ x, long long rows, int rotate,
+                                                         const unsigned int* __restrict__ amax_bits,
+                                                         uint8_t* __restrict__ codes) {
+  constexpr int E = D / 32;
+  const float amax = __uint_as_float(*amax_bits);
+  const float delta = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  const long long warps = static_cast<long long>(gridDim.x) * 8;
+  for (long long row = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row < rows; row += warps) {
+    float v[E];
+    load_row_rotated<D>(x, row, rotate != 0, v);
+    uint8_t* dst = codes + row * D + lane_id() * E;
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta),
+                                                      __fdiv_rn(v[2], delta), __fdiv_rn(v[3], delta));
+    } else {
+      const uint32_t w = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta), 0.f, 0.f);
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w & 0xffffu);
+    }
+  }
+}
+
+__global__ void fp8q_delta_kernel(float* __restrict__ descale) {
+  const float amax = __uint_as_float(*reinterpret_cast<const unsigned int*>(descale));
+  *descale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+}
+
+template <int D, typename T>
+fa_status launch_impl(const void* x, int rotate, void* codes, float* descale, long long rows, cudaStream_t s) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = (rows + 7) / 8;
+  if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
+  if (blocks < 1) blocks = 1;
+  if (cudaMemsetAsync(descale, 0, sizeof(float), s) != cudaSuccess) return FA_ERR_LAUNCH;
+  unsigned int* amax_bits = reinterpret_cast<unsigned int*>(descale);  // holds max |y| until the last step
+  fp8q_amax_kernel<D, T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const T*>(x), rows, rotate,
+                                                                        amax_bits);
+  fp8q_codes_kernel<D, T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const T*>(x), rows, rotate,
+                                                                         amax_bits, static_cast<uint8_t*>(codes));
+  fp8q_delta_kernel<<<1, 1, 0, s>>>(descale);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+fa_status launch_fp8_quantize(const void* x, int x_dtype, int rotate, void* codes, float* descale, long long rows,
+                              int d, cudaStream_t s) {
+  if (d == 64)
+    return x_dtype == 1 ? launch_impl<64, __nv_bfloat16>(x, rotate, codes, descale, rows, s)
+                        : launch_impl<64, float>(x, rotate, codes, descale, rows, s);
+  return x_dtype == 1 ? launch_impl<128, __nv_bfloat16>(x, rotate, codes, descale, rows, s)
+                      : launch_impl<128, float>(x, rotate, codes, descale, rows, s);
+}
+
+}  // namespace fa

@@ -54,6 +54,8 @@ fa_status launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 fa_status launch_bwd_dq_convert(const float* dq_acc, void* dq, long long rows, int d, float scale,
                                 cudaStream_t stream);
 fa_status launch_timeout_probe(unsigned int limit_us, cudaStream_t stream);
+fa_status launch_fp8_quantize(const void* x, int x_dtype, int rotate, void* codes, float* descale, long long rows,
+                              int d, cudaStream_t stream);
 
 // Reads and clears each translation unit's device error word (stream-ordered
 // copy followed by a stream synchronisation done by the caller).

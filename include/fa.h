@@ -125,6 +125,24 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
                      int d, int causal, float scale, void* stream);
 
 /*
+ * FP8 storage for fa_fwd_fp8 ("FLASH-ATTN", FlashAttention-3 > Low-precision
+ * with FP8: one scale per tensor, and incoherent processing -- Q and K are
+ * multiplied by an orthogonal matrix before quantisation, which leaves QK^T
+ * unchanged and spreads outliers; the matrix is a Hadamard transform as in
+ * "FlashAttention 三代演进", 技术 4).
+ *   x       : rows x d input, fp32 (x_dtype = 0) or bf16 (x_dtype = 1), device.
+ *   hadamard: 1 to rotate each row by H/sqrt(d) (H the Sylvester Hadamard
+ *             matrix; use it for Q and K, never for V), 0 to quantise as is.
+ *   codes   : rows x d e4m3 codes out (1 byte each), device.
+ *   descale : one fp32 out, device: delta = max|y| / 448 (1 if all zero), so
+ *             that y ~= delta * code.
+ *   d in {64, 128}; rows >= 1.  Three launches on `stream`; the descale word
+ *   holds the running maximum until the last one.
+ */
+fa_status fa_fp8_quantize(const void* x, int x_dtype, int hadamard, void* codes, float* descale, long long rows,
+                          int d, void* stream);
+
+/*
  * fa_bwd without a workspace argument, for callers that cannot allocate
  * device memory: a plugin inside another runtime that is handed only its
  * input and output tensors, or code on a path where cudaMalloc (which can

@@ -12,6 +12,9 @@ from .attention import (  # noqa: F401
     flops_forward,
     forward,
     forward_fp8_reference,
+    hadamard_matrix,
+    quantize_e4m3_reference,
+    rotate_rows,
     head_backward,
     head_forward,
     head_forward_online,

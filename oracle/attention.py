@@ -245,3 +245,43 @@ def flops_forward(B: int, H: int, N: int, d: int, causal: bool) -> float:
 def flops_backward(B: int, H: int, N: int, d: int, causal: bool) -> float:
     """2.5 x the forward: five products against two."""
     return 2.5 * flops_forward(B, H, N, d, causal)
+
+
+# ---------------------------------------------------------------------------
+# FP8 storage with incoherent processing.
+# ---------------------------------------------------------------------------
+
+def hadamard_matrix(d: int) -> np.ndarray:
+    """Sylvester Hadamard matrix of order d (a power of two), scaled by 1/sqrt(d)
+    so that it is orthogonal: H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]].
+
+    "FLASH-ATTN", FlashAttention-3 > Low-precision with FP8 (incoherent
+    processing multiplies Q and K by an orthogonal matrix M, which leaves
+    (QM)(KM)^T = QK^T) and "FlashAttention 三代演进", 技术 4 (the matrix is a
+    Hadamard transform).
+    """
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    if h.shape[0] != d:
+        raise ValueError("d must be a power of two")
+    return h / math.sqrt(d)
+
+
+def rotate_rows(x, d_axis_last=True):
+    """x @ H for the last dimension (float64)."""
+    x = _f64(x)
+    return x @ hadamard_matrix(x.shape[-1])
+
+
+def quantize_e4m3_reference(x):
+    """Per-tensor e4m3 storage ("FLASH-ATTN", Low-precision with FP8: one scale
+    per tensor): delta = amax|x| / 448 and code = e4m3_rne(x / delta).  The
+    rounding is torch's float8_e4m3fn conversion (round to nearest even), applied
+    to the float32 value of x / delta.  Returns (codes as uint8, delta)."""
+    import torch
+    x = _f64(x)
+    amax = float(np.abs(x).max())
+    delta = amax / 448.0 if amax > 0 else 1.0
+    y = torch.from_numpy(np.clip(x / delta, -448.0, 448.0)).to(torch.float32)
+    return y.to(torch.float8_e4m3fn).view(torch.uint8).numpy(), delta

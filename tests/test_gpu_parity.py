@@ -191,6 +191,50 @@ def test_fp8_forward_vs_unquantised_per_tensor_only(causal):
     assert e <= FP8_O_REL_FRO, f"FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
 
 
+def _e4m3_codes(t):
+    return torch.from_numpy(np.clip(t, -448.0, 448.0).astype(np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("hadamard", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_fp8_quantize_matches_reference(hadamard, d, dtype):
+    # The code is an integer decided in floating point: the kernel rotates in
+    # fp32 and the reference in fp64, so a code may differ only where y/delta
+    # lies within 2e-6 (relative) of an e4m3 rounding boundary.
+    x = inputs.draw_outlier_fp32(1, 2, 300, d, seed=7)[0].to(dtype)
+    codes, dsc = api.fa_fp8_quantize(x.cuda(), hadamard)
+    torch.cuda.synchronize()
+    y = oracle.rotate_rows(x) if hadamard else f64(x)
+    ref_codes, ref_delta = oracle.quantize_e4m3_reference(y)
+    delta = float(dsc.item())
+    assert abs(delta - ref_delta) <= 1e-6 * ref_delta
+    got = codes.cpu().numpy()
+    t = y / ref_delta
+    ok = (got == ref_codes) | (got == _e4m3_codes(t * (1 - 2e-6))) | (got == _e4m3_codes(t * (1 + 2e-6)))
+    assert ok.all()
+    assert (got == ref_codes).mean() > 0.999
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [256, 1000])
+def test_fp8_forward_with_incoherent_processing(causal, N):
+    # Q and K rotated by the Hadamard transform before per-tensor e4m3
+    # storage (V as is), against exact attention on the unquantised inputs.
+    B, H, d = 1, 2, 128
+    q, k, v = inputs.draw_outlier_fp32(B, H, N, d, seed=4)
+    scale = 1 / math.sqrt(d)
+    q8, dsq = api.fa_fp8_quantize(q.cuda(), True)
+    k8, dsk = api.fa_fp8_quantize(k.cuda(), True)
+    v8, dsv = api.fa_fp8_quantize(v.cuda(), False)
+    o, lse = api.fa_fwd_fp8(q8, k8, v8, dsq, dsk, dsv, causal, scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.forward_fp8_reference(q, k, v, causal, scale)
+    e = rel_fro(f64(o), o_ref)
+    assert e <= FP8_O_REL_FRO, f"FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
+
+
 # ---------------------------------------------------------------- errors and the timeout path
 
 def test_timeout_path_reports_and_context_survives():

@@ -309,3 +309,42 @@ def test_fp8_quantisation_roundtrip():
     big = x.abs() > 2 ** -6 * delta * 4
     rel = ((deq - x).abs() / x.abs())[big]
     assert float(rel.max()) <= 2 ** -4 + 1e-6
+
+
+# ---------------------------------------------------------------- FP8 storage
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_hadamard_is_orthogonal_with_plus_minus_entries(d):
+    h = oracle.hadamard_matrix(d)
+    np.testing.assert_allclose(h @ h.T, np.eye(d), rtol=0, atol=1e-13)
+    assert np.all(np.abs(np.abs(h) * math.sqrt(d) - 1.0) < 1e-15)
+    # Sylvester order: row 0 is constant, row 1 alternates sign
+    assert np.all(h[0] > 0) and np.all(h[1, ::2] > 0) and np.all(h[1, 1::2] < 0)
+
+
+def test_hadamard_rotation_leaves_attention_unchanged():
+    q, k, v = rand_qkv(40, 64, 31)
+    o1, l1, _ = oracle.head_forward(q, k, v, True, 0.125)
+    o2, l2, _ = oracle.head_forward(oracle.rotate_rows(q), oracle.rotate_rows(k), v, True, 0.125)
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-12)
+
+
+def test_hadamard_spreads_a_single_outlier():
+    x = np.zeros((1, 128))
+    x[0, 5] = 10.0
+    y = oracle.rotate_rows(x)
+    np.testing.assert_allclose(np.abs(y), 10.0 / math.sqrt(128), rtol=1e-15)
+
+
+def test_e4m3_reference_quantiser():
+    x = rng(32).standard_normal((64, 128)) * 3.0
+    codes, delta = oracle.quantize_e4m3_reference(x)
+    assert abs(delta - np.abs(x).max() / 448.0) < 1e-15
+    deq = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy() * delta
+    # the amax entry maps to 448 exactly; normals are within half an e4m3 ulp (2^-4 relative)
+    assert abs(np.abs(deq).max() - np.abs(x).max()) <= 1e-12 * np.abs(x).max()
+    big = np.abs(x) >= 2.0 ** -6 * delta
+    assert np.all(np.abs(deq - x)[big] <= 2.0 ** -4 * np.abs(x)[big] + 1e-15)
+    # e4m3 codes 0x7F / 0xFF are NaN: never produced
+    assert not np.any((codes & 0x7F) == 0x7F)
