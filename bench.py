@@ -125,6 +125,23 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (x itself on one process)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, ms_slowest: float) -> float:
+    """Work of all ranks (independent replicas) over the slowest rank's time."""
+    return world * flops_per_step * steps / (ms_slowest * 1e-3) / 1e12
+
+
 def cpu_oracle_sample(heads, N, d, causal, seed):
     """Times the float64 oracle (forward + backward) on `heads` heads of the
     workload; returns (seconds, flops of those heads)."""
@@ -186,7 +203,10 @@ def run_ours(args):
         _build.build()
     if world > 1:
         dist.barrier()
-    W = WORKLOAD
+    W = dict(WORKLOAD)
+    if args.shape:  # profiling cases only; the default is the workload above
+        W["B"], W["H"], W["N"], W["d"] = (int(x) for x in args.shape.split(","))
+        W["name"] = f"causal_B{W['B']}_H{W['H']}_N{W['N']}_d{W['d']}"
     B, H, N, d, causal = W["B"], W["H"], W["N"], W["d"], W["causal"]
     scale = 1.0 / math.sqrt(d)
     q, k, v, do = inputs.draw_bf16(B, H, N, d, W["seed"])
@@ -238,17 +258,14 @@ def run_ours(args):
         dist.barrier()
     ms_total = start.elapsed_time(stop)
     per_kernel = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j, n in enumerate(kernels)}
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, "cuda")
     if api.fa_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
     fwd_fl, bwd_fl = flops_step(B, H, N, d, causal)
     step_fl = fwd_fl + bwd_fl
     ms_step = ms_total / args.steps
-    value = world * step_fl * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(world, step_fl, args.steps, ms_total)
 
     # ---- end to end through the same API with pinned host buffers
     hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
@@ -266,22 +283,21 @@ def run_ours(args):
         for h, dvc in ((ho, o), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
             h.copy_(dvc, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
+    ms_e2e = float("nan")
+    if not args.no_e2e:
         e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    e2e_value = world * step_fl * e2e_steps / (ms_e2e * 1e-3) / 1e12
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = e0.elapsed_time(e1)
+    ms_e2e = max_over_ranks(ms_e2e, "cuda") if not args.no_e2e else ms_e2e
+    e2e_value = None if args.no_e2e else whole_job_tflops(world, step_fl, e2e_steps, ms_e2e)
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = measured_peaks()
@@ -319,8 +335,8 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "kernels": kernel_stats,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+        "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                                               "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
     }
@@ -344,6 +360,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--shape", default="", help="B,H,N,d of a causal profiling case instead of the workload")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
