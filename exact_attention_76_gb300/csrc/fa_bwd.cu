@@ -287,22 +287,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so the key-row warpgroup computes P_(i+1) while dK_i and dQ_i run.
     if (elect_one()) {
       const uint32_t sm = smem_u32(smem);
-      const uint32_t k_addr = sm + C::kOffK, v_addr = sm + C::kOffV, ds_addr = sm + C::kOffDS;
-      const uint32_t do_addr = sm + C::kOffDO;
+      // Base descriptors (K-major "_k", MN-major "_mn"); operands below advance
+      // them by byte offsets that are compile-time constants after unrolling.
+      const uint64_t k_k = sdesc_sw128(sm + C::kOffK, 16, 1024), k_mn = sdesc_sw128(sm + C::kOffK, C::kBlockBytes, 1024);
+      const uint64_t v_k = sdesc_sw128(sm + C::kOffV, 16, 1024);
+      const uint64_t ds_k = sdesc_sw128(sm + C::kOffDS, 16, 1024), ds_mn = sdesc_sw128(sm + C::kOffDS, C::kBlockBytes, 1024);
+      const uint64_t do_k = sdesc_sw128(sm + C::kOffDO, 16, 1024), do_mn = sdesc_sw128(sm + C::kOffDO, C::kBlockBytes, 1024);
+      const uint64_t q_k = sdesc_sw128(sm + C::kOffQ, 16, 1024), q_mn = sdesc_sw128(sm + C::kOffQ, C::kBlockBytes, 1024);
       auto issue_s = [&](int i) {  // S^T = K Q_i^T
-        const uint32_t q_addr = sm + C::kOffQ + (i & 1) * C::kTileBytes;
+        const uint64_t qb = sdesc_advance(q_k, (i & 1) * C::kTileBytes);
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::kTmS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
-                      C::kIdescKK, kk > 0);
+          mma_bf16_ss(tmem + C::kTmS, sdesc_advance(k_k, off), sdesc_advance(qb, off), C::kIdescKK, kk > 0);
         }
         tc_commit(&sh.s_full);
       };
       auto issue_dp = [&]() {  // dP^T = V dO_i^T
+#pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::kTmDP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
-                      C::kIdescKK, kk > 0);
+          mma_bf16_ss(tmem + C::kTmDP, sdesc_advance(v_k, off), sdesc_advance(do_k, off), C::kIdescKK, kk > 0);
         }
         tc_commit(&sh.dp_full);
       };
@@ -319,15 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it & 1;
-        const uint32_t q_addr = sm + C::kOffQ + st * C::kTileBytes;
+        const uint64_t qm = sdesc_advance(q_mn, st * C::kTileBytes);
         const bool has_next = it + 1 < n_it;
         // dV += P_i^T dO_i
         ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
         if (!ok) break;
         tc_fence_after();
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmS + kk * 8, sdesc_sw128(do_addr + kk * 2048, C::kBlockBytes, 1024),
-                      C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmS + kk * 8, sdesc_advance(do_mn, kk * 2048), C::kIdescKM,
+                      (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sh.dv_done);
         tc_commit(&sh.do_empty);
         // S_(i+1): its columns hold P_i^T until dV_i has read them.
@@ -342,10 +348,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&sh.ds_ready, it & 1, &sh.abort, &g_err_bwd);
         if (!ok) break;
         tc_fence_after();
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::kTmDK, sdesc_sw128(ds_addr + off, 16, 1024),
-                      sdesc_sw128(q_addr + kk * 2048, C::kBlockBytes, 1024), C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ss(tmem + C::kTmDK, sdesc_advance(ds_k, off), sdesc_advance(qm, kk * 2048), C::kIdescKM,
+                      (it > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&sh.q_empty[st]);
         if (D == 64 && it > 0) {  // separate dQ columns: only the previous read-out must be done
@@ -353,9 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
         }
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tmem + C::kTmDQ, sdesc_sw128(ds_addr + kk * 2048, C::kBlockBytes, 1024),
-                      sdesc_sw128(k_addr + kk * 2048, C::kBlockBytes, 1024), C::kIdescMM, kk > 0);
+          mma_bf16_ss(tmem + C::kTmDQ, sdesc_advance(ds_mn, kk * 2048), sdesc_advance(k_mn, kk * 2048), C::kIdescMM,
+                      kk > 0);
         tc_commit(&sh.dq_full);
         // dP_(i+1)
         if (has_next) {

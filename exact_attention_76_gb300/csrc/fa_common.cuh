@@ -259,6 +259,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Descriptor of the same operand layout starting `byte_off` bytes further:
+// the start address sits in the low 14 bits as address >> 4 and shared-memory
+// addresses stay below 256 KB, so the offset adds without carrying out.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t byte_off) {
+  return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32 D.
 // Bits: D format (4-5) = 1 (f32); A format (7-9) = 1 (bf16); B format (10-12)
 // = 1 (bf16); A major (15), B major (16): 0 = K-major, 1 = MN-major;

@@ -5,30 +5,37 @@
 // a running row sum l of exp(S - m) and an UNSCALED output accumulator
 // O~ = sum_j exp(S_j - m) V_j; O = diag(l)^-1 O~ and L = m + log(l) are formed
 // once after the loop.  Fully masked blocks of a causal row block are never
-// visited and only the diagonal block applies the element mask (same
-// section).  Query blocks are independent thread blocks (> Parallelism).
+// visited and only the blocks that cross the diagonal apply the element mask
+// (same section).  Query blocks are independent thread blocks (> Parallelism).
 //
 // How it maps to the SM (one CTA = 256 query rows of one (batch, head)):
 //  * warps 0-3 and 4-7: two softmax warpgroups, one per 128-row query tile;
 //    thread r of a warpgroup owns row r (TMEM lane r);
-//  * warp 8: TMA producer -- the two Q tiles once, then K_j and V_j into a
-//    ring of shared-memory slots guarded by full/empty mbarriers (the
-//    producer/consumer split of "FLASH-ATTN", FlashAttention-3 >
+//  * warp 8: TMA producer -- the two Q tiles once, then K_j and V_j (64 keys
+//    each) into a ring of shared-memory slots guarded by full/empty mbarriers
+//    (the producer/consumer split of "FLASH-ATTN", FlashAttention-3 >
 //    Producer-Consumer asynchrony);
 //  * warp 9: allocates TMEM and, from one thread, issues every tcgen05.mma:
 //    S_t = Q_t K_j^T (both operands in shared memory) and O_t += P_t V_j with
-//    P_t read from TMEM, where the softmax warpgroup wrote it over S_t.
-// The MMA order per key block j is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
-// each warpgroup's softmax overlaps the other tile's two products (the
-// ping-pong of two consumer warpgroups, "FLASH-ATTN", FlashAttention-3).
+//    P_t read from TMEM.
+//
+// Each query tile has its own S, P and O columns in TMEM, so the next S_t can
+// be computed as soon as the softmax warpgroup has copied the current S_t into
+// registers, while it is still exponentiating; the products of the other tile
+// fill the tensor pipe meanwhile (the two-stage and ping-pong overlaps of
+// "FLASH-ATTN", FlashAttention-3).  Per key block j and tile t the single MMA
+// thread issues S_t(j+1) (after the warpgroup released S_t(j)) and then
+// PV_t(j) (after it wrote P_t(j)).
 //
 // Softmax works in the log2 domain: x = S * (scale * log2 e) with one FMA, then
 // ex2.  The reference maximum m_used is raised only when a block's maximum
 // exceeds it by more than TAU (8 for bf16, i.e. values up to 2^8 before a
-// rescale; 0 for e4m3, whose P must stay <= 1); raising it rescales l and
-// the warpgroup's own O row in TMEM.  Any TAU gives the same exact result.
+// rescale; 0 for e4m3, whose P must stay <= 1); raising it rescales l and the
+// warpgroup's own O row in TMEM once the previous PV has completed.  Any TAU
+// gives the same exact result.
 //
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D).
+// TMEM columns: S_0 [0,64), S_1 [64,128), P_0 from 128, P_1 from 160,
+// O_0 [256,256+D), O_1 [256+D,256+2D).
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
@@ -42,34 +49,42 @@ __device__ uint32_t g_err_fwd;
 
 constexpr int kThreads = 320;
 constexpr int kBM = 128;  // query rows per tile (one TMEM lane each)
-constexpr int kBN = 128;  // keys per key/value block
+constexpr int kBN = 64;   // keys per key/value block
 
 template <int D, bool FP8>
 struct FwdCfg {
   static constexpr int kElemBytes = FP8 ? 1 : 2;
-  static constexpr int kRowBytes = D * kElemBytes;     // bytes of one row of Q/K/V
-  static constexpr int kColBlocks = kRowBytes / 128;   // 128-byte column blocks
-  static constexpr int kBoxCols = 128 / kElemBytes;    // elements per TMA box row
-  static constexpr int kTileBytes = 128 * kRowBytes;   // one 128-row tile
-  static constexpr int kBlockBytes = 128 * 128;        // one column block of a tile
-  static constexpr int kSlots = (kTileBytes >= 32768) ? 4 : 8;
-  static constexpr int kSmemBytes = 2 * kTileBytes + kSlots * kTileBytes + 1024;
-  static constexpr int kKPerMma = FP8 ? 32 : 16;       // K extent of one MMA
-  static constexpr int kQKSteps = kRowBytes / 32;      // MMAs for S = Q K^T
-  static constexpr int kPVSteps = kBN / kKPerMma;      // MMAs for O += P V
+  static constexpr int kRowBytes = D * kElemBytes;       // bytes of one row of Q/K/V
+  static constexpr int kColBlocks = kRowBytes / 128;     // 128-byte column blocks
+  static constexpr int kBoxCols = 128 / kElemBytes;      // elements per TMA box row
+  static constexpr int kQBlockBytes = kBM * 128;         // one column block of a Q tile
+  static constexpr int kQTileBytes = kBM * kRowBytes;
+  static constexpr int kKVBlockBytes = kBN * 128;        // one column block of a K/V tile
+  static constexpr int kKVTileBytes = kBN * kRowBytes;
+  static constexpr int kSlots = 131072 / kKVTileBytes;   // 128 KB ring
+  static constexpr int kSmemBytes = 2 * kQTileBytes + kSlots * kKVTileBytes + 1024;
+  static constexpr int kKPerMma = FP8 ? 32 : 16;         // K extent of one MMA
+  static constexpr int kQKSteps = kRowBytes / 32;        // MMAs for S = Q K^T
+  static constexpr int kPVSteps = kBN / kKPerMma;        // MMAs for O += P V
   static constexpr float kTauLog2 = FP8 ? 0.0f : 8.0f;
   static constexpr float kPScale = FP8 ? 256.0f : 1.0f;
   static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(128, kBN, false, false) : idesc_bf16(128, kBN, false, false);
   static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
+  static constexpr uint32_t kTmS = 0;     // + t * kBN
+  static constexpr uint32_t kTmP = 128;   // + t * 32
+  static constexpr uint32_t kTmO = 256;   // + t * D
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(kColBlocks >= 1, "row must fill a 128-byte swizzle row");
+  static_assert(kSlots <= 16, "barrier arrays");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct FwdSmem {
   uint64_t q_full;
-  uint64_t kv_full[8];
-  uint64_t kv_empty[8];
+  uint64_t kv_full[16];
+  uint64_t kv_empty[16];
   uint64_t s_full[2];
+  uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t drain;
@@ -98,8 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmem sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_q = smem;                       // two Q tiles
-  uint8_t* s_kv = smem + 2 * C::kTileBytes;  // ring of K/V slots
+  uint8_t* s_q = smem;                        // two Q tiles
+  uint8_t* s_kv = smem + 2 * C::kQTileBytes;  // ring of K/V slots
 
   // A wait of an earlier CTA ran out: the launch is already failed, stop here
   // (the word stays set until fa_device_error reads and clears it).
@@ -118,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int t = 0; t < 2; ++t) {
     const int row0 = q0 + t * kBM;
     if (row0 >= N) n_t[t] = 0;
-    else n_t[t] = causal ? min(n_kv_all, row0 / kBN + 1) : n_kv_all;
+    else n_t[t] = causal ? min(n_kv_all, (row0 + kBM - 1) / kBN + 1) : n_kv_all;
   }
   const int n_max = max(n_t[0], n_t[1]);
 
@@ -131,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sh.s_full[t], 1);
+      mbar_init(&sh.s_free[t], kBM);
       mbar_init(&sh.p_full[t], kBM);
       mbar_init(&sh.o_done[t], 1);
     }
@@ -149,10 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(&sh.q_full, 2 * C::kTileBytes);
+      mbar_arrive_expect_tx(&sh.q_full, 2 * C::kQTileBytes);
       for (int t = 0; t < 2; ++t)
         for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d(s_q + t * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * C::kBoxCols, q0 + t * kBM, bh,
+          tma_load_3d(s_q + t * C::kQTileBytes + cb * C::kQBlockBytes, &map_q, cb * C::kBoxCols, q0 + t * kBM, bh,
                       &sh.q_full);
       int issued = 0;
       for (int j = 0; j < n_max && !sh.abort.flag; ++j) {
@@ -160,10 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = issued % C::kSlots;
           const int round = issued / C::kSlots;
           if (round > 0 && !mbar_wait<true>(&sh.kv_empty[slot], (round - 1) & 1, &sh.abort, &g_err_fwd)) break;
-          mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
+          mbar_arrive_expect_tx(&sh.kv_full[slot], C::kKVTileBytes);
           const CUtensorMap* m = kv == 0 ? &map_k : &map_v;
           for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(s_kv + slot * C::kTileBytes + cb * C::kBlockBytes, m, cb * C::kBoxCols, j * kBN, bh,
+            tma_load_3d(s_kv + slot * C::kKVTileBytes + cb * C::kKVBlockBytes, m, cb * C::kBoxCols, j * kBN, bh,
                         &sh.kv_full[slot]);
           ++issued;
         }
@@ -181,77 +197,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one() && n_max > 0) {
-      const uint32_t q_addr = smem_u32(s_q);
-      const uint32_t kv_addr = smem_u32(s_kv);
+      // Base descriptors; every operand below is one of these advanced by a
+      // byte offset that is a compile-time constant after unrolling.
+      const uint64_t q_desc = sdesc_sw128(smem_u32(s_q), 16, 1024);                     // K-major Q tiles
+      const uint64_t k_desc = sdesc_sw128(smem_u32(s_kv), 16, 1024);                    // K-major K slots
+      const uint64_t v_desc = sdesc_sw128(smem_u32(s_kv), C::kKVBlockBytes, 1024);      // MN-major V slots
       auto issue_s = [&](int t, int slot) {
-        const uint32_t a0 = q_addr + t * C::kTileBytes;
-        const uint32_t b0 = kv_addr + slot * C::kTileBytes;
+        const uint64_t a0 = sdesc_advance(q_desc, t * C::kQTileBytes);
+        const uint64_t b0 = sdesc_advance(k_desc, slot * C::kKVTileBytes);
+#pragma unroll
         for (int kk = 0; kk < C::kQKSteps; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          issue_mma(FP8, tmem + t * kBN, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
-                    C::kIdescS, kk > 0);
+          const uint32_t in_row = (kk & 3) * 32;
+          issue_mma(FP8, tmem + C::kTmS + t * kBN, sdesc_advance(a0, (kk >> 2) * C::kQBlockBytes + in_row),
+                    sdesc_advance(b0, (kk >> 2) * C::kKVBlockBytes + in_row), C::kIdescS, kk > 0);
         }
+        tc_commit(&sh.s_full[t]);
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint32_t b0 = kv_addr + slot * C::kTileBytes;
-        for (int kk = 0; kk < C::kPVSteps; ++kk) {
-          issue_mma_ts(FP8, tmem + 256 + t * D, tmem + t * kBN + kk * 8,
-                       sdesc_sw128(b0 + kk * C::kKPerMma * 128, C::kBlockBytes, 1024), C::kIdescPV,
+        const uint64_t b0 = sdesc_advance(v_desc, slot * C::kKVTileBytes);
+        const uint32_t a_tm = tmem + C::kTmP + t * 32;
+        const uint32_t d_tm = tmem + C::kTmO + t * D;
+#pragma unroll
+        for (int kk = 0; kk < C::kPVSteps; ++kk)
+          issue_mma_ts(FP8, d_tm, a_tm + kk * 8, sdesc_advance(b0, kk * C::kKPerMma * 128), C::kIdescPV,
                        (acc || kk > 0) ? 1u : 0u);
-        }
+        tc_commit(&sh.o_done[t]);
       };
-      bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd);
       auto wait_load = [&](int idx) {
         return mbar_wait<true>(&sh.kv_full[idx % C::kSlots], (idx / C::kSlots) & 1, &sh.abort, &g_err_fwd);
       };
-      if (ok) ok = wait_load(0);
+      bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd) && wait_load(0);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) {
-            issue_s(t, 0);
-            tc_commit(&sh.s_full[t]);
-          }
+          if (n_t[t] > 0) issue_s(t, 0);
         tc_commit(&sh.kv_empty[0]);
       }
       for (int j = 0; ok && j < n_max; ++j) {
-        const int v_idx = 2 * j + 1;
-        const int k_idx = 2 * j + 2;
-        ok = wait_load(v_idx);
-        const bool has_next = (j + 1 < n_max);
-        bool k_ready = false;
+        const int k_idx = 2 * j + 2;  // K_(j+1)
+        const int v_idx = 2 * j + 1;  // V_j
+        bool k_ready = false, v_ready = false;
         for (int t = 0; ok && t < 2; ++t) {
-          if (j < n_t[t]) {
-            ok = mbar_wait<true>(&sh.p_full[t], j & 1, &sh.abort, &g_err_fwd);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, v_idx % C::kSlots, j > 0);
-            tc_commit(&sh.o_done[t]);
-          }
-          if (t == 1) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
-          if (has_next && j + 1 < n_t[t]) {
+          // S_t(j+1): its columns are free once the warpgroup copied S_t(j) out.
+          if (j + 1 < n_t[t]) {
             if (!k_ready) {
               ok = wait_load(k_idx);
-              if (!ok) break;
-              tc_fence_after();
               k_ready = true;
             }
-            // P_t(j) lives in S_t's columns: S_t(j+1) may only be written
-            // once PV_t(j) has read it.
-            ok = mbar_wait<true>(&sh.o_done[t], j & 1, &sh.abort, &g_err_fwd);
+            ok = ok && mbar_wait<true>(&sh.s_free[t], j & 1, &sh.abort, &g_err_fwd);
             if (!ok) break;
             tc_fence_after();
             issue_s(t, k_idx % C::kSlots);
-            tc_commit(&sh.s_full[t]);
           }
-        }
-        if (ok && has_next) {
-          if (!k_ready) {  // no tile needed K_{j+1}: cannot happen, kept for safety
-            ok = wait_load(k_idx);
+          // PV_t(j) once the warpgroup wrote P_t(j).
+          if (j < n_t[t]) {
+            if (!v_ready) {
+              ok = wait_load(v_idx);
+              v_ready = true;
+            }
+            ok = ok && mbar_wait<true>(&sh.p_full[t], j & 1, &sh.abort, &g_err_fwd);
+            if (!ok) break;
             tc_fence_after();
+            issue_pv(t, v_idx % C::kSlots, j > 0);
           }
-          tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
         }
+        if (!ok) break;
+        if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
+        if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
       }
       // Teardown: every MMA issued by this thread completes before TMEM is freed.
       tc_commit(&sh.drain);
@@ -263,8 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;              // query tile of this warpgroup
     const int r = threadIdx.x & 127;      // row within the tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_col = tmem + lane_base + t * kBN;
-    const uint32_t o_col = tmem + lane_base + 256 + t * D;
+    const uint32_t s_col = tmem + lane_base + C::kTmS + t * kBN;
+    const uint32_t p_col = tmem + lane_base + C::kTmP + t * 32;
+    const uint32_t o_col = tmem + lane_base + C::kTmO + t * D;
     const int row_g = q0 + t * kBM + r;
     const int nt = n_t[t];
     float c = scale_log2;
@@ -282,15 +295,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[kBN];
       {
-        uint32_t rr[32];
+        uint32_t ra[32], rb[32];
+        tmem_ld32(s_col, ra);
+        tmem_ld32(s_col + 32, rb);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
 #pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          tmem_ld32(s_col + cc * 32, rr);
-          tmem_ld_wait(rr);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(rr[i]);
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(ra[i]);
+          s[32 + i] = __uint_as_float(rb[i]);
         }
       }
+      tc_fence_before();
+      mbar_arrive(&sh.s_free[t]);  // S_t(j+1) may now be written
       const int key0 = j * kBN;
       const bool need_mask = (causal && key0 + kBN - 1 > q0 + t * kBM) || (key0 + kBN > N);
       if (need_mask) {
@@ -303,15 +320,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
       const float m_cand = mx * c;
+      float alpha = 1.0f;
+      bool raise = false;
       if (j == 0) {
         m_used = m_cand;
-      } else {
-        const bool raise = m_cand > m_used + C::kTauLog2;
+      } else if (m_cand > m_used + C::kTauLog2) {
+        raise = true;
+        alpha = ex2_approx(m_used - m_cand);
+        m_used = m_cand;
+      }
+      const float neg_m = -m_used;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < kBN; ++i) {
+        s[i] = ex2_approx(fmaf(s[i], c, neg_m));
+        part[i & 3] += s[i];
+      }
+      l_sum = l_sum * alpha + ((part[0] + part[1]) + (part[2] + part[3]));
+      // PV_t(j-1) must be complete before P_t(j) overwrites P_t(j-1) and before
+      // O_t is rescaled.
+      if (j > 0) {
+        ok = mbar_wait<true>(&sh.o_done[t], (j - 1) & 1, &sh.abort, &g_err_fwd);
+        if (!ok) break;
+        tc_fence_after();
         if (__any_sync(0xffffffffu, raise)) {
-          const float alpha = raise ? ex2_approx(m_used - m_cand) : 1.0f;
-          if (raise) m_used = m_cand;
-          l_sum *= alpha;
-          // O_t(j-1) is complete: S_t(j) was issued only after PV_t(j-1) finished.
 #pragma unroll 1
           for (int cc = 0; cc < D; cc += 32) {
             uint32_t rr[32];
@@ -323,29 +355,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const float neg_m = -m_used;
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < kBN; ++i) {
-        s[i] = ex2_approx(fmaf(s[i], c, neg_m));
-        part[i & 3] += s[i];
-      }
-      l_sum += (part[0] + part[1]) + (part[2] + part[3]);
       if (FP8) {
-        uint32_t pw[32];
+        uint32_t pw[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 16; ++i)
           pw[i] = pack_e4m3x4(s[4 * i] * C::kPScale, s[4 * i + 1] * C::kPScale, s[4 * i + 2] * C::kPScale,
                               s[4 * i + 3] * C::kPScale);
-        tmem_st32(s_col, pw);
+        tmem_st16(p_col, pw);
       } else {
+        uint32_t pw[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pw[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]);
-          tmem_st32(s_col + h * 32, pw);
-        }
+        for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+        tmem_st32(p_col, pw);
       }
       tmem_st_wait();
       tc_fence_before();
