@@ -262,10 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 4; ++u) {
         const int r = lane * 4 + u;
         const int qg = qrow0 + r;
-        float l2 = INFINITY, dd = 0.f;
+        float l2 = -INFINITY, dd = -0.f;  // stored negated: -L log2 e and -D
         if (qg < N) {
-          l2 = __ldg(lse + static_cast<size_t>(bh) * N + qg) * kLog2e;
-          dd = __ldg(dvec + static_cast<size_t>(bh) * N + qg);
+          l2 = __ldg(lse + static_cast<size_t>(bh) * N + qg) * -kLog2e;
+          dd = -__ldg(dvec + static_cast<size_t>(bh) * N + qg);
         }
         s_lse2[st * 128 + r] = l2;
         s_dvec[st * 128 + r] = dd;
@@ -405,15 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait(rr);
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {  // L for 4 queries per 16-byte broadcast load
-          const float4 lq = reinterpret_cast<const float4*>(l2)[cc * 8 + i4];
-          const float lv[4] = {lq.x, lq.y, lq.z, lq.w};
+          const float4 lq = reinterpret_cast<const float4*>(l2)[cc * 8 + i4];  // -L log2 e
+          const int i = i4 * 4;
+          const float2 c2 = make_float2(scale_log2, scale_log2);
+          const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])), c2,
+                                        make_float2(lq.x, lq.y));
+          const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])), c2,
+                                        make_float2(lq.z, lq.w));
+          const float xv[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int i = i4 * 4 + u;
-            const int q = cc * 32 + i;
-            float x = ex2_approx(fmaf(__uint_as_float(rr[i]), scale_log2, -lv[u]));
-            if (diag && q < r) x = 0.f;  // query before key: masked
-            p[q] = x;
+            const int q = cc * 32 + i + u;
+            p[q] = (diag && q < r) ? 0.f : xv[u];  // query before key: masked
           }
         }
       }
@@ -441,12 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t w[16];
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) {  // D for 4 queries per 16-byte broadcast load
-          const float4 dq4 = reinterpret_cast<const float4*>(dd)[cc * 8 + i2];
+          const float4 dq4 = reinterpret_cast<const float4*>(dd)[cc * 8 + i2];  // -D
           const int q0 = cc * 32 + 4 * i2;
-          w[2 * i2] = pack_bf16x2(p[q0] * (__uint_as_float(rr[4 * i2]) - dq4.x),
-                                  p[q0 + 1] * (__uint_as_float(rr[4 * i2 + 1]) - dq4.y));
-          w[2 * i2 + 1] = pack_bf16x2(p[q0 + 2] * (__uint_as_float(rr[4 * i2 + 2]) - dq4.z),
-                                      p[q0 + 3] * (__uint_as_float(rr[4 * i2 + 3]) - dq4.w));
+          const float2 a = __fmul2_rn(make_float2(p[q0], p[q0 + 1]),
+                                      __fadd2_rn(make_float2(__uint_as_float(rr[4 * i2]), __uint_as_float(rr[4 * i2 + 1])),
+                                                 make_float2(dq4.x, dq4.y)));
+          const float2 b = __fmul2_rn(make_float2(p[q0 + 2], p[q0 + 3]),
+                                      __fadd2_rn(make_float2(__uint_as_float(rr[4 * i2 + 2]), __uint_as_float(rr[4 * i2 + 3])),
+                                                 make_float2(dq4.z, dq4.w)));
+          w[2 * i2] = pack_bf16x2(a.x, a.y);
+          w[2 * i2 + 1] = pack_bf16x2(b.x, b.y);
         }
         uint8_t* blk = ds_row + (cc >> 1) * C::kBlockBytes;
 #pragma unroll

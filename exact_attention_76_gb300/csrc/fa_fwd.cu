@@ -329,14 +329,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = ex2_approx(m_used - m_cand);
         m_used = m_cand;
       }
-      const float neg_m = -m_used;
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 c2 = make_float2(c, c);
+      const float2 nm2 = make_float2(-m_used, -m_used);
+      float2 part0 = make_float2(0.f, 0.f), part1 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < kBN; ++i) {
-        s[i] = ex2_approx(fmaf(s[i], c, neg_m));
-        part[i & 3] += s[i];
+      for (int i = 0; i < kBN; i += 4) {
+        const float2 x0 = __ffma2_rn(make_float2(s[i], s[i + 1]), c2, nm2);
+        const float2 x1 = __ffma2_rn(make_float2(s[i + 2], s[i + 3]), c2, nm2);
+        s[i] = ex2_approx(x0.x);
+        s[i + 1] = ex2_approx(x0.y);
+        s[i + 2] = ex2_approx(x1.x);
+        s[i + 3] = ex2_approx(x1.y);
+        part0 = __fadd2_rn(part0, make_float2(s[i], s[i + 1]));
+        part1 = __fadd2_rn(part1, make_float2(s[i + 2], s[i + 3]));
       }
-      l_sum = l_sum * alpha + ((part[0] + part[1]) + (part[2] + part[3]));
+      l_sum = l_sum * alpha + ((part0.x + part0.y) + (part1.x + part1.y));
       // PV_t(j-1) must be complete before P_t(j) overwrites P_t(j-1) and before
       // O_t is rescaled.
       if (j > 0) {
