@@ -31,6 +31,8 @@ SIGNATURES = {
     "fa_status_string": ([_I], ctypes.c_char_p),
     "fa_device_error": ([_P], _I),
     "fa_debug_wait_timeout": ([_U, _P], _I),
+    "fa_fwd_gqa": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
+    "fa_bwd_gqa": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "fa_fp8_quantize": ([_P, _I, _I, _P, _P, _L, _I, _P], _I),
     "fa_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
 }

@@ -130,16 +130,22 @@ using namespace fa;
 
 extern "C" {
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-                 int causal, float scale, void* stream) {
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+                     int d, int causal, float scale, void* stream) {
   fa_status st;
   if ((st = check_ptrs(q, k, v, o, lse)) != FA_OK) return st;
   if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if (Hkv <= 0 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((st = check_device()) != FA_OK) return st;
-  FwdArgs a{q, k, v, o, lse, nullptr, nullptr, nullptr, B, H, N, d, causal, scale};
+  FwdArgs a{q, k, v, o, lse, nullptr, nullptr, nullptr, B, H, N, d, causal, scale, Hkv};
   return launch_fwd_bf16(a, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                 int causal, float scale, void* stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, N, d, causal, scale, stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
@@ -167,7 +173,7 @@ fa_status fa_bwd_main(const void* q, const void* k, const void* v, const float* 
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((st = check_device()) != FA_OK) return st;
-  BwdArgs a{q, k, v, lse, dO, D, dq_acc, dk, dv, B, H, N, d, causal, scale};
+  BwdArgs a{q, k, v, lse, dO, D, dq_acc, dk, dv, B, H, N, d, causal, scale, H};
   return launch_bwd_main(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -181,12 +187,13 @@ fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, 
                                static_cast<cudaStream_t>(stream));
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                 int causal, float scale, void* stream) {
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                     int N, int d, int causal, float scale, void* stream) {
   fa_status st;
   if ((st = check_ptrs(q, k, v, o, lse, dO, dq, dk, dv)) != FA_OK) return st;
   if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if (Hkv <= 0 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   const size_t need = fa_bwd_workspace_size(B, H, N, d);
@@ -198,9 +205,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round16(rows * sizeof(float)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = launch_bwd_preprocess(o, dO, Dvec, dq_acc, static_cast<long long>(rows), d, s)) != FA_OK) return st;
-  BwdArgs a{q, k, v, lse, dO, Dvec, dq_acc, dk, dv, B, H, N, d, causal, scale};
+  BwdArgs a{q, k, v, lse, dO, Dvec, dq_acc, dk, dv, B, H, N, d, causal, scale, Hkv};
   if ((st = launch_bwd_main(a, s)) != FA_OK) return st;
   return launch_bwd_dq_convert(dq_acc, dq, static_cast<long long>(rows), d, scale, s);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                 void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                 int causal, float scale, void* stream) {
+  return fa_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, H, H, N, d, causal, scale,
+                    stream);
 }
 
 fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale_q,
@@ -214,7 +228,7 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((st = check_device()) != FA_OK) return st;
-  FwdArgs a{q8, k8, v8, o, lse, descale_q, descale_k, descale_v, B, H, N, d, causal, scale};
+  FwdArgs a{q8, k8, v8, o, lse, descale_q, descale_k, descale_v, B, H, N, d, causal, scale, H};
   return launch_fwd_fp8(a, static_cast<cudaStream_t>(stream));
 }
 

@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse,
                        const float* __restrict__ dvec, __nv_bfloat16* __restrict__ dk_out,
                        __nv_bfloat16* __restrict__ dv_out, int BH, int N, int causal, float scale,
-                       float scale_log2, int head_group) {
+                       float scale_log2, int head_group, int H, int qgroup) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   static_assert(sizeof(BwdBars) <= 256, "barrier block");
@@ -182,10 +182,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id();
   const int n_blk = (N + 127) / 128;
+  // bh: the K/V head of this CTA (BH of them); its query heads are the
+  // `qgroup` consecutive heads qh0 .. qh0 + qgroup - 1 (grouped-query
+  // attention; qgroup = 1 when every query head has its own K/V head).
   int bh, kb;
   bwd_item(static_cast<int>(blockIdx.x), BH, n_blk, head_group, bh, kb);
+  const int hkv = H / qgroup;
+  const int qh0 = (bh / hkv) * H + (bh % hkv) * qgroup;
   const int i_begin = causal ? kb : 0;
-  const int n_it = n_blk - i_begin;
+  const int n_per = n_blk - i_begin;  // query blocks per query head
+  const int n_it = qgroup * n_per;
+  // Every role walks the same (query head, query block) sequence: query
+  // blocks i_begin .. n_blk-1 of head qh0, then of qh0 + 1, and so on.
+  struct QCursor {
+    int i, h;
+  };
+  auto q_advance = [&](QCursor& c, int it) {
+    if (it > 0 && ++c.i == n_blk) {
+      c.i = i_begin;
+      ++c.h;
+    }
+  };
 
   if (threadIdx.x == 0) {
     sh.abort.flag = 0;
@@ -229,11 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int q_issued[2] = {0, 0};
     int do_issued = 0;
+    QCursor cur{i_begin, qh0};
     for (int it = 0; it < n_it; ++it) {
+      q_advance(cur, it);
       if (__shfl_sync(0xffffffffu, sh.abort.flag, 0)) break;  // one decision for the whole warp
       const int st = it & 1;
       const int use = it >> 1;
-      const int qrow0 = (i_begin + it) * 128;
+      const int qrow0 = cur.i * 128;
+      const int qh = cur.h;
       bool ok = true;
       if (lane == 0) {
         // Q_i: two stages, freed when dK_(i-2) has read it.
@@ -241,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           mbar_arrive_expect_tx(&sh.q_full[st], C::kTileBytes);
           for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * 64, qrow0, bh,
+            tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * 64, qrow0, qh,
                         &sh.q_full[st]);
           ++q_issued[st];
         }
@@ -250,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           mbar_arrive_expect_tx(&sh.do_full, C::kTileBytes);
           for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(smem + C::kOffDO + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, bh, &sh.do_full);
+            tma_load_3d(smem + C::kOffDO + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, qh, &sh.do_full);
           ++do_issued;
         }
       }
@@ -264,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qg = qrow0 + r;
         float l2 = -INFINITY, dd = -0.f;  // stored negated: -L log2 e and -D
         if (qg < N) {
-          l2 = __ldg(lse + static_cast<size_t>(bh) * N + qg) * -kLog2e;
-          dd = -__ldg(dvec + static_cast<size_t>(bh) * N + qg);
+          l2 = __ldg(lse + static_cast<size_t>(qh) * N + qg) * -kLog2e;
+          dd = -__ldg(dvec + static_cast<size_t>(qh) * N + qg);
         }
         s_lse2[st * 128 + r] = l2;
         s_dvec[st * 128 + r] = dd;
@@ -388,7 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ds_row = smem + C::kOffDS + r * 128;
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     bool ok = true;
+    QCursor cur{i_begin, qh0};
     for (int it = 0; it < n_it; ++it) {
+      q_advance(cur, it);
       const int st = it & 1;
       ok = mbar_wait(&sh.ld_full[st], (it >> 1) & 1, &sh.abort, &g_err_bwd) &&
            mbar_wait(&sh.s_full, it & 1, &sh.abort, &g_err_bwd);
@@ -396,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float* l2 = s_lse2 + st * 128;
       const float* dd = s_dvec + st * 128;
-      const bool diag = causal && (i_begin + it == kb);
+      const bool diag = causal && (cur.i == kb);
       float p[128];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -499,7 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = (threadIdx.x == 128);
     bool ok = true;
     bool staged_before = false;
+    QCursor cur{i_begin, qh0};
     for (int it = 0; it < n_it; ++it) {
+      q_advance(cur, it);
       ok = mbar_wait(&sh.dq_full, it & 1, &sh.abort, &g_err_bwd);
       if (!ok) break;
       tc_fence_after();
@@ -514,7 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&sh.dq_free);
-      const int qrow0 = (i_begin + it) * 128;
+      const int qrow0 = cur.i * 128;
+      const int qh = cur.h;
 #pragma unroll
       for (int round = 0; round < C::kDqRounds; ++round) {
         if (staged_before) {
@@ -534,8 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (leader) {
-          tma_reduce_add_3d(&map_dq, round * 64, qrow0, bh, smem + C::kOffStage);
-          tma_reduce_add_3d(&map_dq, round * 64 + 32, qrow0, bh, smem + C::kOffStage + C::kBlockBytes);
+          tma_reduce_add_3d(&map_dq, round * 64, qrow0, qh, smem + C::kOffStage);
+          tma_reduce_add_3d(&map_dq, round * 64 + 32, qrow0, qh, smem + C::kOffStage + C::kBlockBytes);
           bulk_commit_group();
         }
         staged_before = true;
@@ -577,11 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  const int BH = a.B * a.H;
+  const int BHq = a.B * a.H;     // query heads
+  const int BH = a.B * a.Hkv;    // key/value heads: one CTA column each
+  const int qgroup = a.H / a.Hkv;
   CUtensorMap mq, mk, mv, mdo, mdq;
-  if (!encode_rows_map(&mq, a.q, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mk, a.k, 2, D, a.N, BH, 64, 128) ||
-      !encode_rows_map(&mv, a.v, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdo, a.dO, 2, D, a.N, BH, 64, 128) ||
-      !encode_rows_map(&mdq, a.dq_acc, 4, D, a.N, BH, 32, 128))
+  if (!encode_rows_map(&mq, a.q, 2, D, a.N, BHq, 64, 128) || !encode_rows_map(&mk, a.k, 2, D, a.N, BH, 64, 128) ||
+      !encode_rows_map(&mv, a.v, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdo, a.dO, 2, D, a.N, BHq, 64, 128) ||
+      !encode_rows_map(&mdq, a.dq_acc, 4, D, a.N, BHq, 32, 128))
     return FA_ERR_LAUNCH;
   auto kern = fa_bwd_main_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
@@ -589,13 +616,13 @@ fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   const int n_blk = (a.N + 127) / 128;
   // Heads per group: Q, dO (bf16) and the dQ accumulator (fp32) of a group
   // should stay within about 48 MB of the L2.
-  const long long head_bytes = static_cast<long long>(a.N) * D * (2 + 2 + 4);
+  const long long head_bytes = static_cast<long long>(a.N) * D * (2 + 2 + 4) * qgroup;
   int group = static_cast<int>(std::max<long long>(1, (48ll << 20) / head_bytes));
   group = std::min(group, BH);
   dim3 grid(static_cast<unsigned>(n_blk * BH));
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a.lse, a.D,
                                                    static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv),
-                                                   BH, a.N, a.causal, a.scale, a.scale * kLog2e, group);
+                                                   BH, a.N, a.causal, a.scale, a.scale * kLog2e, group, a.H, qgroup);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

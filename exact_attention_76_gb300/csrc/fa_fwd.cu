@@ -30,7 +30,7 @@
 // Softmax works in the log2 domain: x = S * (scale * log2 e) with one FMA, then
 // ex2.  The reference maximum m_used is raised only when a block's maximum
 // exceeds it by more than TAU (8 for bf16, i.e. values up to 2^8 before a
-// rescale; 0 for e4m3, whose P must stay <= 1); raising it rescales l and the
+// rescale; 0.75 for e4m3, whose P * 2^8 must stay below 448); raising it rescales l and the
 // warpgroup's own O row in TMEM once the previous PV has completed.  Any TAU
 // gives the same exact result.
 //
@@ -66,7 +66,9 @@ struct FwdCfg {
   static constexpr int kKPerMma = FP8 ? 32 : 16;         // K extent of one MMA
   static constexpr int kQKSteps = kRowBytes / 32;        // MMAs for S = Q K^T
   static constexpr int kPVSteps = kBN / kKPerMma;        // MMAs for O += P V
-  static constexpr float kTauLog2 = FP8 ? 0.0f : 8.0f;
+  // e4m3 P is stored as P * 2^8 and the largest e4m3 value is 448, so P may
+  // reach 2^0.75 (2^0.75 * 256 = 430.5) before the reference max must move.
+  static constexpr float kTauLog2 = FP8 ? 0.75f : 8.0f;
   static constexpr float kPScale = FP8 ? 256.0f : 1.0f;
   static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(128, kBN, false, false) : idesc_bf16(128, kBN, false, false);
   static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap map_v, __nv_bfloat16* __restrict__ out_o,
                   float* __restrict__ out_lse, const float* __restrict__ descale_q,
                   const float* __restrict__ descale_k, const float* __restrict__ descale_v, int BH, int N,
-                  int causal, float scale_log2) {
+                  int causal, float scale_log2, int H, int qgroup) {
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmem sh;
@@ -126,7 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dispatched first.
   const int item = static_cast<int>(blockIdx.x);
   const int qb = causal ? (n_qblk - 1 - item / BH) : item / BH;
-  const int bh = item % BH;
+  const int bh = item % BH;                       // query head
+  // K/V head of this query head (grouped-query attention: qgroup consecutive
+  // query heads share one; qgroup = 1 otherwise)
+  const int bh_kv = (bh / H) * (H / qgroup) + (bh % H) / qgroup;
   const int q0 = qb * 2 * kBM;
   const int n_kv_all = (N + kBN - 1) / kBN;
   int n_t[2];
@@ -179,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&sh.kv_full[slot], C::kKVTileBytes);
           const CUtensorMap* m = kv == 0 ? &map_k : &map_v;
           for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(s_kv + slot * C::kKVTileBytes + cb * C::kKVBlockBytes, m, cb * C::kBoxCols, j * kBN, bh,
+            tma_load_3d(s_kv + slot * C::kKVTileBytes + cb * C::kKVBlockBytes, m, cb * C::kBoxCols, j * kBN, bh_kv,
                         &sh.kv_full[slot]);
           ++issued;
         }
@@ -418,10 +423,11 @@ template <int D, bool FP8>
 fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D, FP8>;
   const int BH = a.B * a.H;
+  const int BHkv = a.B * a.Hkv;
   CUtensorMap mq, mk, mv;
   if (!encode_rows_map(&mq, a.q, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBM) ||
-      !encode_rows_map(&mk, a.k, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBN) ||
-      !encode_rows_map(&mv, a.v, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBN))
+      !encode_rows_map(&mk, a.k, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN) ||
+      !encode_rows_map(&mv, a.v, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN))
     return FA_ERR_LAUNCH;
   auto kern = fa_fwd_kernel<D, FP8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
@@ -429,7 +435,8 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(((a.N + 2 * kBM - 1) / (2 * kBM)) * BH));
   const float scale_log2 = a.scale * 1.4426950408889634f;
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.descale_q,
-                                                   a.descale_k, a.descale_v, BH, a.N, a.causal, scale_log2);
+                                                   a.descale_k, a.descale_v, BH, a.N, a.causal, scale_log2, a.H,
+                                                   a.H / a.Hkv);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -29,6 +29,7 @@ struct FwdArgs {
   int B, H, N, d;
   int causal;
   float scale;
+  int Hkv;  // key/value heads; H % Hkv == 0 (H for plain multi-head attention)
 };
 
 struct BwdArgs {
@@ -44,6 +45,7 @@ struct BwdArgs {
   int B, H, N, d;
   int causal;
   float scale;
+  int Hkv;  // key/value heads of k, v, dk, dv; H % Hkv == 0
 };
 
 fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);

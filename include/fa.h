@@ -65,6 +65,18 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int causal, float scale, void* stream);
 
 /*
+ * Grouped-query forward ("FLASH-ATTN", FlashAttention-2 > FlashAttention-2,
+ * multi-query and grouped-query attention: several query heads share one key
+ * head and one value head, addressed by adjusting the head index instead of
+ * copying K and V).  As fa_fwd, with
+ *   q, o : [B,H,N,d] bf16;  k, v : [B,Hkv,N,d] bf16;  lse : [B,H,N] fp32,
+ *   Hkv >= 1 dividing H; query head h uses key/value head h / (H / Hkv).
+ * fa_fwd(...) is fa_fwd_gqa with Hkv = H.
+ */
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+                     int d, int causal, float scale, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: D ([B,H,N] fp32, 16-byte padded)
  * followed by the fp32 dQ accumulator ([B,H,N,d]).  0 on invalid sizes.
  */
@@ -87,6 +99,20 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                  int causal, float scale, void* stream);
+
+/*
+ * Grouped-query backward (same section: the gradients of a shared key or
+ * value head are the sums over the query heads that use it).  As fa_bwd, with
+ *   q, o, dO, dq : [B,H,N,d] bf16;  k, v, dk, dv : [B,Hkv,N,d] bf16;
+ *   lse : [B,H,N] fp32;  Hkv >= 1 dividing H;
+ *   workspace : fa_bwd_workspace_size(B, H, N, d) bytes (per query head).
+ * Each CTA owns one key/value head's block of keys and loops over all query
+ * heads of its group, so dK and dV are summed on chip without atomics.
+ * fa_bwd(...) is fa_bwd_gqa with Hkv = H.
+ */
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                     int N, int d, int causal, float scale, void* stream);
 
 /*
  * Backward step 1: D_i = sum_k dO_ik O_ik (fp32), which equals
@@ -117,8 +143,9 @@ fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, 
  *   descale_q, descale_k, descale_v : DEVICE pointers to one fp32 each (delta).
  *   o   : [B,H,N,d] bf16 out, O = softmax(scale * (dq dk) q8 k8^T) (dv v8).
  *   lse : [B,H,N] fp32 out, natural-log LogSumExp of the scaled logits.
- * Inside, P is stored as e4m3 times 2^8 for the second product; the factor is
- * removed in the final division by the row sum.
+ * Inside, P is stored as e4m3 times 2^8 for the second product (P <= 2^0.75,
+ * so P * 2^8 stays below 448); the factor is removed in the final division
+ * by the row sum.
  */
 fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale_q,
                      const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H, int N,

@@ -8,10 +8,12 @@ does not re-use its own formula.
 from .attention import (  # noqa: F401
     LN2,
     backward,
+    backward_gqa,
     flops_backward,
     flops_forward,
     forward,
     forward_fp8_reference,
+    forward_gqa,
     hadamard_matrix,
     quantize_e4m3_reference,
     rotate_rows,

@@ -285,3 +285,34 @@ def quantize_e4m3_reference(x):
     delta = amax / 448.0 if amax > 0 else 1.0
     y = torch.from_numpy(np.clip(x / delta, -448.0, 448.0)).to(torch.float32)
     return y.to(torch.float8_e4m3fn).view(torch.uint8).numpy(), delta
+
+
+# ---------------------------------------------------------------------------
+# Grouped-query attention.
+# ---------------------------------------------------------------------------
+
+def _expand_kv(x, H):
+    """[B, Hkv, N, d] -> [B, H, N, d]: query head h reads key/value head
+    h // (H // Hkv) ("FLASH-ATTN", FlashAttention-2 > FlashAttention-2: the
+    shared heads are addressed by index, not copied; copying here is the plain
+    definition)."""
+    x = _f64(x)
+    return np.repeat(x, H // x.shape[1], axis=1)
+
+
+def forward_gqa(q, k, v, causal: bool, scale: float, heads=None):
+    """Grouped-query forward: standard attention with each query head reading
+    its group's key and value head."""
+    H = _f64(q).shape[1]
+    return forward(q, _expand_kv(k, H), _expand_kv(v, H), causal, scale, heads=heads)
+
+
+def backward_gqa(q, k, v, do, causal: bool, scale: float):
+    """Grouped-query backward: per query head as in `backward`, then dK and dV
+    of a shared head summed over the query heads that read it (same section)."""
+    H = _f64(q).shape[1]
+    Hkv = _f64(k).shape[1]
+    dq, dk, dv = backward(q, _expand_kv(k, H), _expand_kv(v, H), do, causal, scale)
+    B, _, N, d = dk.shape
+    g = H // Hkv
+    return dq, dk.reshape(B, Hkv, g, N, d).sum(axis=2), dv.reshape(B, Hkv, g, N, d).sum(axis=2)

@@ -120,6 +120,31 @@ def test_large_logits_rescale_path():
     check_bwd(dq, dk, dv, q, k, v, do, False, 0.125)
 
 
+# ---------------------------------------------------------------- grouped-query attention
+
+@pytest.mark.parametrize("H,Hkv,N,d,causal", [
+    (4, 1, 256, 128, True),    # multi-query: every query head shares one K/V head
+    (6, 2, 333, 64, False),    # ragged tail
+    (8, 4, 512, 128, True),
+    (4, 2, 130, 64, True),
+])
+def test_gqa_forward_backward(H, Hkv, N, d, causal):
+    B = 2
+    q, _, _, do = inputs.draw_bf16(B, H, N, d, seed=H * 100 + N)
+    _, k, v, _ = inputs.draw_bf16(B, Hkv, N, d, seed=Hkv * 100 + N + 1)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    o, lse = api.fa_fwd_gqa(qd, kd, vd, causal, scale)
+    dq, dk, dv = api.fa_bwd_gqa(qd, kd, vd, o, lse, dod, causal, scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.forward_gqa(q, k, v, causal, scale)
+    assert max_abs(f64(o), o_ref) <= O_MAX_ABS
+    assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
+    for name, got, ref in zip(("dQ", "dK", "dV"), (dq, dk, dv), oracle.backward_gqa(q, k, v, do, causal, scale)):
+        e = rel_fro(f64(got), ref)
+        assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e}"
+
+
 # ---------------------------------------------------------------- step by step
 
 def test_preprocess_and_convert_steps():

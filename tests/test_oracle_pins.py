@@ -348,3 +348,40 @@ def test_e4m3_reference_quantiser():
     assert np.all(np.abs(deq - x)[big] <= 2.0 ** -4 * np.abs(x)[big] + 1e-15)
     # e4m3 codes 0x7F / 0xFF are NaN: never produced
     assert not np.any((codes & 0x7F) == 0x7F)
+
+
+# ---------------------------------------------------------------- grouped-query attention
+
+def test_gqa_with_one_query_head_per_kv_head_is_plain_attention():
+    q, k, v, do = (t.double().numpy() for t in inputs.draw_fp32(1, 4, 24, 8, 5))
+    o1, l1 = oracle.forward(q, k, v, True, 0.3)
+    o2, l2 = oracle.forward_gqa(q, k, v, True, 0.3)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_gradients_by_central_differences(causal):
+    # Two query heads share one key/value head: the gradient of the loss with
+    # respect to the shared K and V must include both heads' contributions.
+    r = rng(41)
+    q = r.standard_normal((1, 2, 6, 4))
+    k = r.standard_normal((1, 1, 6, 4))
+    v = r.standard_normal((1, 1, 6, 4))
+    do = r.standard_normal((1, 2, 6, 4))
+    s, h = 0.5, 1e-6
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.forward_gqa(qq, kk, vv, causal, s)
+        return float((o * do).sum())
+
+    dq, dk, dv = oracle.backward_gqa(q, k, v, do, causal, s)
+    for x, g, idx in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+        fd = np.zeros_like(x)
+        for pos in np.ndindex(x.shape):
+            xp = x.copy(); xp[pos] += h
+            xm = x.copy(); xm[pos] -= h
+            a_p = [q, k, v]; a_p[idx] = xp
+            a_m = [q, k, v]; a_m[idx] = xm
+            fd[pos] = (loss(*a_p) - loss(*a_m)) / (2 * h)
+        assert np.abs(fd - g).max() <= 1e-6 * max(1.0, np.abs(g).max()), idx
