@@ -147,14 +147,25 @@ struct BwdBars {
 
 // Block index -> (head, key block).  Heads are taken in groups whose Q, dO
 // and dQ accumulator fit in L2 together; within a group the key blocks with
-// the most query blocks (causal: the lowest) come first.
+// the most query blocks (causal: the lowest) come first.  A partial group (the
+// remainder of BH / group) goes first, so that every later group runs long
+// enough to absorb its own heaviest blocks and the launch ends on light ones.
 __device__ __forceinline__ void bwd_item(int item, int BH, int n_blk, int group, int& bh, int& kb) {
-  const int per_group = group * n_blk;
-  const int g = item / per_group;
-  const int r = item - g * per_group;
-  const int g_heads = min(group, BH - g * group);
+  const int rem = BH % group;
+  int g_heads, base_item, base_head;
+  if (item < rem * n_blk) {
+    g_heads = rem;
+    base_item = 0;
+    base_head = 0;
+  } else {
+    const int g = (item - rem * n_blk) / (group * n_blk);
+    g_heads = group;
+    base_item = rem * n_blk + g * group * n_blk;
+    base_head = rem + g * group;
+  }
+  const int r = item - base_item;
   kb = r / g_heads;
-  bh = g * group + (r - kb * g_heads);
+  bh = base_head + (r - kb * g_heads);
 }
 
 template <int D>
