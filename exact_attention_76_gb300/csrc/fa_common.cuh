@@ -155,6 +155,16 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, int x,
       "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src))
       : "memory");
 }
+// 3-D tiled store of a shared-memory tile to global memory; box rows past the
+// tensor's extent are not written.  Tracked by the issuing thread's bulk
+// async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, const void* smem_src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
+      " [%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src))
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk group of this thread has finished READING
 // shared memory (the source buffer may be overwritten afterwards).
@@ -340,6 +350,17 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // Named barrier among `nthreads` threads (multiple of 32) with id 1..15.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also returns the AND of `v` over the participating threads.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pin, pout;\n setp.ne.u32 pin, %1, 0;\n"
+      " barrier.cta.red.and.pred pout, %2, %3, pin;\n selp.u32 %0, 1, 0, pout;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ----------------------------------------------------------------- math

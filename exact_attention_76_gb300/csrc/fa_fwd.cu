@@ -59,6 +59,8 @@ struct FwdCfg {
   static constexpr int kBoxCols = 128 / kElemBytes;      // elements per TMA box row
   static constexpr int kQBlockBytes = kBM * 128;         // one column block of a Q tile
   static constexpr int kQTileBytes = kBM * kRowBytes;
+  static constexpr int kOColBlocks = D * 2 / 128;                // 128-byte column blocks of a bf16 O row
+  static constexpr int kOStageBlocks = kQTileBytes / kQBlockBytes;  // O blocks that fit in a Q tile
   static constexpr int kKVBlockBytes = kBN * 128;        // one column block of a K/V tile
   static constexpr int kKVTileBytes = kBN * kRowBytes;
   static constexpr int kSlots = 131072 / kKVTileBytes;   // 128 KB ring
@@ -78,6 +80,7 @@ struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(kColBlocks >= 1, "row must fill a 128-byte swizzle row");
   static_assert(kSlots <= 16, "barrier arrays");
+  static_assert(kOStageBlocks >= 1 && kOColBlocks % kOStageBlocks == 0, "O staging");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -107,7 +110,7 @@ __device__ __forceinline__ void issue_mma_ts(bool fp8, uint32_t d, uint32_t a, u
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, __nv_bfloat16* __restrict__ out_o,
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                   float* __restrict__ out_lse, const float* __restrict__ descale_q,
                   const float* __restrict__ descale_k, const float* __restrict__ descale_v, int BH, int N,
                   int causal, float scale_log2, int H, int qgroup) {
@@ -384,30 +387,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&sh.p_full[t]);
     }
-    if (ok && nt > 0) {
-      ok = mbar_wait<true>(&sh.o_done[t], (nt - 1) & 1, &sh.abort, &g_err_fwd);
-      tc_fence_after();
+    // Epilogue: O = O~ / l in bf16, staged with the 128-byte swizzle in this
+    // tile's own Q space and written by TMA stores, which drop box rows past N.
+    // The Q tile is dead here: the MMA thread issued the tile's last S product
+    // before its last PV, so the o_done completion covers it.  Every thread of
+    // the warpgroup takes every barrier below, so a failed wait in one of them
+    // cannot leave the others waiting; a store is issued only if all were fine.
+    if (nt > 0) {
       if (ok) {
-        const float inv = o_mult / l_sum;
-        const bool store = row_g < N;
-        __nv_bfloat16* dst = out_o + (static_cast<size_t>(bh) * N + (store ? row_g : 0)) * D;
-#pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t rr[32];
-          tmem_ld32(o_col + cc, rr);
-          tmem_ld_wait(rr);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
-          if (store) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
-        if (store) out_lse[static_cast<size_t>(bh) * N + row_g] = m_used * 0.69314718055994531f + logf(l_sum);
+        ok = mbar_wait<true>(&sh.o_done[t], (nt - 1) & 1, &sh.abort, &g_err_fwd);
+        tc_fence_after();
       }
+      const float inv = o_mult / l_sum;
+      uint8_t* stage = s_q + t * C::kQTileBytes;
+      const uint32_t sw = static_cast<uint32_t>(r & 7);
+      const bool leader = r == 0;
+#pragma unroll 1
+      for (int ob = 0; ob < C::kOColBlocks; ob += C::kOStageBlocks) {
+        if (ob > 0) {  // the staging space is reused: earlier stores must have read it
+          if (leader) bulk_wait_read_all();
+          named_bar_sync(1 + t, kBM);
+        }
+        if (ok) {
+#pragma unroll
+          for (int b = 0; b < C::kOStageBlocks; ++b) {
+            uint8_t* row_base = stage + b * C::kQBlockBytes + r * 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t rr[32];
+              tmem_ld32(o_col + (ob + b) * 64 + h * 32, rr);
+              tmem_ld_wait(rr);
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4*>(row_base + (((h * 4 + i) ^ sw) << 4)) =
+                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        ok = named_bar_and(1 + t, kBM, ok);
+        if (ok && leader) {
+#pragma unroll
+          for (int b = 0; b < C::kOStageBlocks; ++b)
+            tma_store_3d(&map_o, (ob + b) * 64, q0 + t * kBM, bh, stage + b * C::kQBlockBytes);
+          bulk_commit_group();
+        }
+      }
+      if (leader) bulk_wait_read_all();  // shared memory must outlive the stores' reads
+      if (ok && row_g < N)
+        out_lse[static_cast<size_t>(bh) * N + row_g] = m_used * 0.69314718055994531f + logf(l_sum);
     }
   }
 
@@ -424,8 +456,9 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D, FP8>;
   const int BH = a.B * a.H;
   const int BHkv = a.B * a.Hkv;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!encode_rows_map(&mq, a.q, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBM) ||
+      !encode_rows_map(&mo, a.o, 2, D, a.N, BH, 64, kBM) ||
       !encode_rows_map(&mk, a.k, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN) ||
       !encode_rows_map(&mv, a.v, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN))
     return FA_ERR_LAUNCH;
@@ -434,7 +467,7 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
     return FA_ERR_LAUNCH;
   dim3 grid(static_cast<unsigned>(((a.N + 2 * kBM - 1) / (2 * kBM)) * BH));
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(a.o), a.lse, a.descale_q,
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a.lse, a.descale_q,
                                                    a.descale_k, a.descale_v, BH, a.N, a.causal, scale_log2, a.H,
                                                    a.H / a.Hkv);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
