@@ -35,7 +35,10 @@
 // gives the same exact result.
 //
 // TMEM columns: S_0 [0,64), S_1 [64,128), P_0 from 128, P_1 from 160,
-// O_0 [256,256+D), O_1 [256+D,256+2D).
+// Q_0 from 192 (Q_1 from 224 when a Q row is 128 bytes), O_0 [256,256+D),
+// O_1 [256+D,256+2D).  A tile whose Q sits in TMEM reads only K from shared
+// memory for S = Q K^T; with both operands in shared memory an M=128, N=64
+// product is bound by shared-memory bandwidth rather than by the tensor core.
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
@@ -77,15 +80,23 @@ struct FwdCfg {
   static constexpr uint32_t kTmS = 0;     // + t * kBN
   static constexpr uint32_t kTmP = 128;   // + t * 32
   static constexpr uint32_t kTmO = 256;   // + t * D
+  // Q kept in TMEM (A operand of S read from TMEM instead of shared memory):
+  // one row of Q needs kRowBytes / 4 columns; tile 0 always fits in the free
+  // columns [192, 256), tile 1 too when a row is at most 128 bytes.
+  static constexpr int kQCols = kRowBytes / 4;
+  static constexpr uint32_t kTmQ = 192;   // + t * kQCols
+  static constexpr bool kQTm1 = kQCols <= 32;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(kColBlocks >= 1, "row must fill a 128-byte swizzle row");
   static_assert(kSlots <= 16, "barrier arrays");
+  static_assert(kTmQ + (kQTm1 ? 2 : 1) * kQCols <= kTmO, "TMEM columns for Q");
   static_assert(kOStageBlocks >= 1 && kOColBlocks % kOStageBlocks == 0, "O staging");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct FwdSmem {
   uint64_t q_full;
+  uint64_t q_tm[2];
   uint64_t kv_full[16];
   uint64_t kv_empty[16];
   uint64_t s_full[2];
@@ -148,6 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     sh.abort.flag = 0;
     mbar_init(&sh.q_full, 1);
+    mbar_init(&sh.q_tm[0], kBM);
+    mbar_init(&sh.q_tm[1], kBM);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(&sh.kv_full[s], 1);
       mbar_init(&sh.kv_empty[s], 1);
@@ -211,13 +224,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t k_desc = sdesc_sw128(smem_u32(s_kv), 16, 1024);                    // K-major K slots
       const uint64_t v_desc = sdesc_sw128(smem_u32(s_kv), C::kKVBlockBytes, 1024);      // MN-major V slots
       auto issue_s = [&](int t, int slot) {
-        const uint64_t a0 = sdesc_advance(q_desc, t * C::kQTileBytes);
         const uint64_t b0 = sdesc_advance(k_desc, slot * C::kKVTileBytes);
+        if (t == 0 || C::kQTm1) {  // Q from TMEM: only K is read from shared memory
+          const uint32_t a_tm = tmem + C::kTmQ + t * C::kQCols;
 #pragma unroll
-        for (int kk = 0; kk < C::kQKSteps; ++kk) {
-          const uint32_t in_row = (kk & 3) * 32;
-          issue_mma(FP8, tmem + C::kTmS + t * kBN, sdesc_advance(a0, (kk >> 2) * C::kQBlockBytes + in_row),
-                    sdesc_advance(b0, (kk >> 2) * C::kKVBlockBytes + in_row), C::kIdescS, kk > 0);
+          for (int kk = 0; kk < C::kQKSteps; ++kk)
+            issue_mma_ts(FP8, tmem + C::kTmS + t * kBN, a_tm + kk * 8,
+                         sdesc_advance(b0, (kk >> 2) * C::kKVBlockBytes + (kk & 3) * 32), C::kIdescS, kk > 0);
+        } else {
+          const uint64_t a0 = sdesc_advance(q_desc, t * C::kQTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < C::kQKSteps; ++kk) {
+            const uint32_t in_row = (kk & 3) * 32;
+            issue_mma(FP8, tmem + C::kTmS + t * kBN, sdesc_advance(a0, (kk >> 2) * C::kQBlockBytes + in_row),
+                      sdesc_advance(b0, (kk >> 2) * C::kKVBlockBytes + in_row), C::kIdescS, kk > 0);
+          }
         }
         tc_commit(&sh.s_full[t]);
       };
@@ -237,9 +258,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd) && wait_load(0);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) issue_s(t, 0);
-        tc_commit(&sh.kv_empty[0]);
+        // Tile 1 first: its Q may come from shared memory, while tile 0's Q is
+        // still being copied into TMEM by its warpgroup.
+        for (int t = 1; ok && t >= 0; --t) {
+          if (n_t[t] == 0) continue;
+          if (t == 0 || C::kQTm1) {
+            ok = mbar_wait<true>(&sh.q_tm[t], 0, &sh.abort, &g_err_fwd);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          issue_s(t, 0);
+        }
+        if (ok) tc_commit(&sh.kv_empty[0]);
       }
       for (int j = 0; ok && j < n_max; ++j) {
         const int k_idx = 2 * j + 2;  // K_(j+1)
@@ -297,6 +327,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY;
     float l_sum = 0.0f;
     bool ok = true;
+    if ((t == 0 || C::kQTm1) && nt > 0) {
+      // Copy this tile's Q rows from shared memory (128-byte swizzle) into its
+      // TMEM columns; the packed words are already in the operand's order.
+      ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd);
+      if (ok) {
+        const uint8_t* src = s_q + t * C::kQTileBytes + r * 128;
+        const uint32_t sw = static_cast<uint32_t>(r & 7);
+        const uint32_t q_col = tmem + lane_base + C::kTmQ + t * C::kQCols;
+#pragma unroll
+        for (int cb = 0; cb < C::kColBlocks; ++cb) {
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + cb * C::kQBlockBytes + ((c ^ sw) << 4));
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+          }
+          tmem_st32(q_col + cb * 32, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sh.q_tm[t]);
+      }
+    }
     for (int j = 0; j < nt; ++j) {
       ok = mbar_wait<true>(&sh.s_full[t], j & 1, &sh.abort, &g_err_fwd);
       if (!ok) break;
