@@ -371,6 +371,35 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 2^x for two values on the FMA pipes (no special-function unit): Cody-Waite
+// reduction x = n + f, n = round(x) by the 1.5 * 2^23 shifter, f in [-1/2, 1/2];
+// 2^f by the degree-DEG polynomial of least maximum relative error on that
+// interval (Remez exchange, coefficients rounded to float32, generated by
+// exp2_minimax.py beside this file); 2^n enters by an integer add into the
+// exponent field.  x is clamped to -126 first so the result stays a normal
+// number (2^-126 in place of smaller values).  Maximum relative error:
+// 1.7e-3 for DEG = 2, 7.5e-5 for DEG = 3.
+template <int DEG>
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  static_assert(DEG == 2 || DEG == 3, "degree");
+  x.x = fmaxf(x.x, -126.0f);
+  x.y = fmaxf(x.y, -126.0f);
+  const float2 t = __fadd2_rn(x, make_float2(12582912.0f, 12582912.0f));
+  const float2 nf = __fadd2_rn(t, make_float2(-12582912.0f, -12582912.0f));
+  const float2 f = __ffma2_rn(nf, make_float2(-1.0f, -1.0f), x);
+  float2 p;
+  if constexpr (DEG == 3) {
+    p = __ffma2_rn(make_float2(0.0551716685f, 0.0551716685f), f, make_float2(0.242611125f, 0.242611125f));
+    p = __ffma2_rn(p, f, make_float2(0.693260968f, 0.693260968f));
+    p = __ffma2_rn(p, f, make_float2(0.999928057f, 0.999928057f));
+  } else {
+    p = __ffma2_rn(make_float2(0.238428935f, 0.238428935f), f, make_float2(0.703447998f, 0.703447998f));
+    p = __ffma2_rn(p, f, make_float2(1.0004431f, 1.0004431f));
+  }
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
   return *reinterpret_cast<uint32_t*>(&h);

@@ -30,9 +30,11 @@
 // Softmax works in the log2 domain: x = S * (scale * log2 e) with one FMA, then
 // ex2.  The reference maximum m_used is raised only when a block's maximum
 // exceeds it by more than TAU (8 for bf16, i.e. values up to 2^8 before a
-// rescale; 0.75 for e4m3, whose P * 2^8 must stay below 448); raising it rescales l and the
-// warpgroup's own O row in TMEM once the previous PV has completed.  Any TAU
-// gives the same exact result.
+// rescale; 0.75 for e4m3, whose P * 2^8 must stay below 448); raising it
+// rescales l and the warpgroup's own O row in TMEM once the previous PV has
+// completed.  Any TAU gives the same exact result.  Each exponential is packed
+// into its P word as soon as it is computed; the e4m3 factor 2^8 is folded
+// into the exponent.
 //
 // TMEM columns: S_0 [0,64), S_1 [64,128), P_0 from 128, P_1 from 160,
 // Q_0 from 192 (Q_1 from 224 when a Q row is 128 bytes), O_0 [256,256+D),
@@ -74,7 +76,21 @@ struct FwdCfg {
   // e4m3 P is stored as P * 2^8 and the largest e4m3 value is 448, so P may
   // reach 2^0.75 (2^0.75 * 256 = 430.5) before the reference max must move.
   static constexpr float kTauLog2 = FP8 ? 0.75f : 8.0f;
-  static constexpr float kPScale = FP8 ? 256.0f : 1.0f;
+  // P goes to the e4m3 operand as P * 2^8: the factor enters the exponent
+  // (m - 8), so the row sum l and O~ both carry it and it cancels in O~ / l.
+  static constexpr float kPShiftLog2 = FP8 ? -8.0f : 0.0f;
+  static constexpr int kPWords = FP8 ? kBN / 4 : kBN / 2;  // 32-bit words of one P row
+  // Exponentials on the FMA pipes ("software exp2"): groups of four (of
+  // kBN / 4) per row and block taken by the polynomial, and its degree (bf16 P
+  // keeps 8 significant bits, e4m3 P 4).  Measured on GB300 it only costs
+  // time: with 2, 4 and 6 of 16 groups the d = 64 forward ran 7, 11 and 18 %
+  // slower and the d = 128 one 0-2 % slower, so no group uses it.
+  static constexpr int kEmuGroups = 0;
+  static constexpr int kPolyDeg = FP8 ? 2 : 3;
+  // Speculative exponentials (below) shorten the softmax when it bounds the
+  // key-block period (bf16 at d = 64: +6 to +8 % measured); at d = 128 the
+  // period is set by the products and the variant measured 2-3 % slower.
+  static constexpr bool kSpecExp = !FP8 && D == 64;
   static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(128, kBN, false, false) : idesc_bf16(128, kBN, false, false);
   static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
   static constexpr uint32_t kTmS = 0;     // + t * kBN
@@ -116,6 +132,41 @@ __device__ __forceinline__ void issue_mma_ts(bool fp8, uint32_t d, uint32_t a, u
                                              uint32_t acc) {
   if (fp8) mma_f8_ts(d, a, b, idesc, acc);
   else mma_bf16_ts(d, a, b, idesc, acc);
+}
+
+// P for one row of a key block: p_i = 2^(s_i * c - m), packed into the words
+// written to TMEM (bf16 pairs, or four e4m3); returns the sum of the p_i.  The
+// scores s are left unchanged.  EMU of the kBN / 4 groups of four use the
+// polynomial exp2 (spread evenly), the rest ex2.approx.
+template <bool FP8, int EMU, int DEG>
+__device__ __forceinline__ float exp2_pack_row(const float (&s)[kBN], float c, float m,
+                                               uint32_t (&pw)[FP8 ? kBN / 4 : kBN / 2]) {
+  const float2 c2 = make_float2(c, c);
+  const float2 nm2 = make_float2(-m, -m);
+  float2 part0 = make_float2(0.f, 0.f), part1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < kBN; i += 4) {
+    const int g = i / 4;
+    const float2 x0 = __ffma2_rn(make_float2(s[i], s[i + 1]), c2, nm2);
+    const float2 x1 = __ffma2_rn(make_float2(s[i + 2], s[i + 3]), c2, nm2);
+    float2 y0, y1;
+    if (((g + 1) * EMU) / (kBN / 4) != (g * EMU) / (kBN / 4)) {
+      y0 = exp2_poly2<DEG>(x0);
+      y1 = exp2_poly2<DEG>(x1);
+    } else {
+      y0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+      y1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+    }
+    part0 = __fadd2_rn(part0, y0);
+    part1 = __fadd2_rn(part1, y1);
+    if constexpr (FP8) {
+      pw[g] = pack_e4m3x4(y0.x, y0.y, y1.x, y1.y);
+    } else {
+      pw[2 * g] = pack_bf16x2(y0.x, y0.y);
+      pw[2 * g + 1] = pack_bf16x2(y1.x, y1.y);
+    }
+  }
+  return (part0.x + part0.y) + (part1.x + part1.y);
 }
 
 template <int D, bool FP8>
@@ -322,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float o_mult = 1.0f;
     if (FP8) {
       c = scale_log2 * __ldg(descale_q) * __ldg(descale_k);
-      o_mult = __ldg(descale_v) / C::kPScale;
+      o_mult = __ldg(descale_v);
     }
     float m_used = -INFINITY;
     float l_sum = 0.0f;
@@ -380,65 +431,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBN; ++i)
           if (key0 + i > lim) s[i] = -INFINITY;
       }
-      float mx = s[0];
-#pragma unroll
-      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
-      const float m_cand = mx * c;
+      uint32_t pw[C::kPWords];
+      float row_sum;
       float alpha = 1.0f;
       bool raise = false;
-      if (j == 0) {
-        m_used = m_cand;
-      } else if (m_cand > m_used + C::kTauLog2) {
-        raise = true;
-        alpha = ex2_approx(m_used - m_cand);
-        m_used = m_cand;
-      }
-      const float2 c2 = make_float2(c, c);
-      const float2 nm2 = make_float2(-m_used, -m_used);
-      float2 part0 = make_float2(0.f, 0.f), part1 = make_float2(0.f, 0.f);
+      if (C::kSpecExp && j > 0 && !need_mask) {
+        // Speculative: P with the current reference maximum, computed while the
+        // block maximum is still being found (the two are independent); only a
+        // row whose block maximum exceeds the reference by more than TAU redoes
+        // it with the raised one.
+        row_sum = exp2_pack_row<FP8, C::kEmuGroups, C::kPolyDeg>(s, c, m_used + C::kPShiftLog2, pw);
+        float mx = s[0];
 #pragma unroll
-      for (int i = 0; i < kBN; i += 4) {
-        const float2 x0 = __ffma2_rn(make_float2(s[i], s[i + 1]), c2, nm2);
-        const float2 x1 = __ffma2_rn(make_float2(s[i + 2], s[i + 3]), c2, nm2);
-        s[i] = ex2_approx(x0.x);
-        s[i + 1] = ex2_approx(x0.y);
-        s[i + 2] = ex2_approx(x1.x);
-        s[i + 3] = ex2_approx(x1.y);
-        part0 = __fadd2_rn(part0, make_float2(s[i], s[i + 1]));
-        part1 = __fadd2_rn(part1, make_float2(s[i + 2], s[i + 3]));
+        for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+        const float m_cand = mx * c;
+        if (m_cand > m_used + C::kTauLog2) {
+          raise = true;
+          alpha = ex2_approx(m_used - m_cand);
+          m_used = m_cand;
+          row_sum = exp2_pack_row<FP8, C::kEmuGroups, C::kPolyDeg>(s, c, m_used + C::kPShiftLog2, pw);
+        }
+      } else {
+        float mx = s[0];
+#pragma unroll
+        for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+        const float m_cand = mx * c;
+        if (j == 0) {
+          m_used = m_cand;
+        } else if (m_cand > m_used + C::kTauLog2) {
+          raise = true;
+          alpha = ex2_approx(m_used - m_cand);
+          m_used = m_cand;
+        }
+        // masked blocks use ex2 throughout, so masked P is exactly 0
+        row_sum = exp2_pack_row<FP8, 0, C::kPolyDeg>(s, c, m_used + C::kPShiftLog2, pw);
       }
-      l_sum = l_sum * alpha + ((part0.x + part0.y) + (part1.x + part1.y));
+      l_sum = l_sum * alpha + row_sum;
       // PV_t(j-1) must be complete before P_t(j) overwrites P_t(j-1) and before
       // O_t is rescaled.
       if (j > 0) {
         ok = mbar_wait<true>(&sh.o_done[t], (j - 1) & 1, &sh.abort, &g_err_fwd);
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, raise)) {
+      }
+      if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-          for (int cc = 0; cc < D; cc += 32) {
-            uint32_t rr[32];
-            tmem_ld32(o_col + cc, rr);
-            tmem_ld_wait(rr);
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t rr[32];
+          tmem_ld32(o_col + cc, rr);
+          tmem_ld_wait(rr);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            tmem_st32(o_col + cc, rr);
-          }
+          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+          tmem_st32(o_col + cc, rr);
         }
       }
-      if (FP8) {
-        uint32_t pw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pw[i] = pack_e4m3x4(s[4 * i] * C::kPScale, s[4 * i + 1] * C::kPScale, s[4 * i + 2] * C::kPScale,
-                              s[4 * i + 3] * C::kPScale);
-        tmem_st16(p_col, pw);
-      } else {
-        uint32_t pw[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-        tmem_st32(p_col, pw);
-      }
+      if constexpr (FP8) tmem_st16(p_col, pw);
+      else tmem_st32(p_col, pw);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sh.p_full[t]);
@@ -495,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (leader) bulk_wait_read_all();  // shared memory must outlive the stores' reads
       if (ok && row_g < N)
-        out_lse[static_cast<size_t>(bh) * N + row_g] = m_used * 0.69314718055994531f + logf(l_sum);
+        out_lse[static_cast<size_t>(bh) * N + row_g] = (m_used + C::kPShiftLog2) * 0.69314718055994531f + logf(l_sum);
     }
   }
 
