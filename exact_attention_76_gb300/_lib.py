@@ -35,6 +35,8 @@ SIGNATURES = {
     "fa_bwd_gqa": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "fa_fp8_quantize": ([_P, _I, _I, _P, _P, _L, _I, _P], _I),
     "fa_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
+    "fa_fwd_fp8_blocks": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P], _I),
+    "fa_fp8_quantize_blocks": ([_P, _I, _I, _I, _P, _P, _I, _I, _I, _P], _I),
 }
 
 _lib = None

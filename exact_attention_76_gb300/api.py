@@ -196,6 +196,56 @@ def fa_fp8_quantize(x, hadamard: bool, codes=None, descale=None, stream=None):
     return codes, descale
 
 
+FP8_BLOCK_Q = 128   # rows of Q per scale (FA_FP8_BLOCK_Q)
+FP8_BLOCK_KV = 64   # rows of K and of V per scale (FA_FP8_BLOCK_KV)
+
+
+def fa_fwd_fp8_blocks(q8, k8, v8, descale_q, descale_k, descale_v, causal: bool, scale: float, o=None, lse=None,
+                      stream=None):
+    """FP8 forward on block-quantised inputs: descale_q is [B*H, ceil(N/128)],
+    descale_k and descale_v are [B*H, ceil(N/64)] fp32 CUDA tensors (one scale
+    per block of rows).  Returns bf16 O and fp32 L."""
+    lib = _lib.load()
+    B, H, N, d = q8.shape
+    for t, n in ((q8, "q8"), (k8, "k8"), (v8, "v8")):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise TypeError(f"{n}: expected e4m3 codes")
+        _check(t, n, t.dtype, (B, H, N, d))
+    nq, nk = -(-N // FP8_BLOCK_Q), -(-N // FP8_BLOCK_KV)
+    _check(descale_q, "descale_q", torch.float32, (B * H, nq))
+    _check(descale_k, "descale_k", torch.float32, (B * H, nk))
+    _check(descale_v, "descale_v", torch.float32, (B * H, nk))
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    _lib.check("fa_fwd_fp8_blocks", lib.fa_fwd_fp8_blocks(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(descale_q),
+                                                          _ptr(descale_k), _ptr(descale_v), _ptr(o), _ptr(lse), B, H,
+                                                          N, d, int(bool(causal)), float(scale),
+                                                          _stream_ptr(stream)))
+    return o, lse
+
+
+def fa_fp8_quantize_blocks(x, hadamard: bool, block_rows: int, codes=None, descale=None, stream=None):
+    """Block e4m3 codes of x [..., N, d] (every leading index one sequence),
+    one scale per block_rows rows of a sequence, optionally after the
+    normalised Hadamard rotation of each row.  Returns (codes uint8 of x's
+    shape, descale fp32 [prod(leading dims), ceil(N / block_rows)])."""
+    lib = _lib.load()
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x: expected fp32 or bf16")
+    _check(x, "x", x.dtype)
+    N, d = x.shape[-2], x.shape[-1]
+    seqs = x.numel() // (N * d)
+    nb = -(-N // int(block_rows))
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if codes is None else codes
+    descale = torch.empty((seqs, nb), dtype=torch.float32, device=x.device) if descale is None else descale
+    _check(codes, "codes", torch.uint8, tuple(x.shape))
+    _check(descale, "descale", torch.float32, (seqs, nb))
+    _lib.check("fa_fp8_quantize_blocks", lib.fa_fp8_quantize_blocks(
+        _ptr(x), 1 if x.dtype == torch.bfloat16 else 0, int(bool(hadamard)), int(block_rows), _ptr(codes),
+        _ptr(descale), seqs, N, d, _stream_ptr(stream)))
+    return codes, descale
+
+
 def fa_status_string(status: int) -> str:
     return _lib.load().fa_status_string(int(status)).decode()
 

@@ -232,6 +232,34 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
   return launch_fwd_fp8(a, static_cast<cudaStream_t>(stream));
 }
 
+fa_status fa_fwd_fp8_blocks(const void* q8, const void* k8, const void* v8, const float* descale_q,
+                            const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H,
+                            int N, int d, int causal, float scale, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(q8, k8, v8, o, lse)) != FA_OK) return st;
+  if (descale_q == nullptr || descale_k == nullptr || descale_v == nullptr) return FA_ERR_INVALID_ARG;
+  if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if ((st = check_device()) != FA_OK) return st;
+  FwdArgs a{q8, k8, v8, o, lse, descale_q, descale_k, descale_v, B, H, N, d, causal, scale, H};
+  return launch_fwd_fp8_blocks(a, static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fp8_quantize_blocks(const void* x, int x_dtype, int hadamard, int block_rows, void* codes,
+                                 float* descale, int seqs, int N, int d, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(x, codes, descale)) != FA_OK) return st;
+  if (seqs <= 0 || seqs > 65535 || N <= 0 || block_rows <= 0 || block_rows > 1024 || (x_dtype != 0 && x_dtype != 1) ||
+      (hadamard != 0 && hadamard != 1) || static_cast<long long>(seqs) * N > (1LL << 31))
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((st = check_device()) != FA_OK) return st;
+  return launch_fp8_quantize_blocks(x, x_dtype, hadamard, block_rows, codes, descale, seqs, N, d,
+                                    static_cast<cudaStream_t>(stream));
+}
+
 fa_status fa_fp8_quantize(const void* x, int x_dtype, int hadamard, void* codes, float* descale, long long rows,
                           int d, void* stream) {
   fa_status st;

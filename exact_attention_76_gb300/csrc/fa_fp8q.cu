@@ -11,8 +11,10 @@
 // One warp per row of d values (d / 32 per lane).  The rotation is a fast
 // Walsh-Hadamard transform: butterflies (a, b) -> (a + b, a - b) over the
 // index bits, first the bits inside a lane's registers, then the lane bits
-// through warp shuffles.  Three launches: max |y| (atomic max on the float's
-// bit pattern, valid for non-negative floats), the codes, and delta.
+// through warp shuffles.  Per tensor: three launches -- max |y| (atomic max on
+// the float's bit pattern, valid for non-negative floats), the codes, and
+// delta.  Per block (block quantisation of the same section: blocks of B_r x d
+// or B_c x d rows, one scale each): one launch, one CTA per block.
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
@@ -122,7 +124,67 @@ fa_status launch_impl(const void* x, int rotate, void* codes, float* descale, lo
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// Block storage: one CTA per (block of block_rows rows, sequence); each warp
+// takes every 8th row of the block, first for max |y|, then for the codes.
+template <int D, typename T>
+__global__ void __launch_bounds__(256) fp8qb_kernel(const T* __restrict__ x, int N, int block_rows, int rotate,
+                                                    uint8_t* __restrict__ codes, float* __restrict__ descale) {
+  constexpr int E = D / 32;
+  __shared__ float s_part[8];
+  const int blk = static_cast<int>(blockIdx.x);
+  const long long seq = blockIdx.y;
+  const int r0 = blk * block_rows;
+  const int r1 = min(N, r0 + block_rows);
+  const long long base = seq * N;
+  float m = 0.f;
+  for (int row = r0 + static_cast<int>(warp_id()); row < r1; row += 8) {
+    float v[E];
+    load_row_rotated<D>(x, base + row, rotate != 0, v);
+#pragma unroll
+    for (int j = 0; j < E; ++j) m = fmaxf(m, fabsf(v[j]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane_id() == 0) s_part[warp_id()] = m;
+  __syncthreads();
+  float amax = s_part[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_part[w]);
+  const float delta = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  if (threadIdx.x == 0) descale[seq * gridDim.x + blk] = delta;
+  for (int row = r0 + static_cast<int>(warp_id()); row < r1; row += 8) {
+    float v[E];
+    load_row_rotated<D>(x, base + row, rotate != 0, v);
+    uint8_t* dst = codes + (base + row) * D + lane_id() * E;
+    if constexpr (E == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta),
+                                                      __fdiv_rn(v[2], delta), __fdiv_rn(v[3], delta));
+    } else {
+      const uint32_t w = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta), 0.f, 0.f);
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w & 0xffffu);
+    }
+  }
+}
+
+template <int D, typename T>
+fa_status launch_blocks_impl(const void* x, int rotate, int block_rows, void* codes, float* descale, int seqs, int N,
+                             cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((N + block_rows - 1) / block_rows), static_cast<unsigned>(seqs));
+  fp8qb_kernel<D, T><<<grid, 256, 0, s>>>(static_cast<const T*>(x), N, block_rows, rotate,
+                                          static_cast<uint8_t*>(codes), descale);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 }  // namespace
+
+fa_status launch_fp8_quantize_blocks(const void* x, int x_dtype, int rotate, int block_rows, void* codes,
+                                     float* descale, int seqs, int N, int d, cudaStream_t s) {
+  if (d == 64)
+    return x_dtype == 1 ? launch_blocks_impl<64, __nv_bfloat16>(x, rotate, block_rows, codes, descale, seqs, N, s)
+                        : launch_blocks_impl<64, float>(x, rotate, block_rows, codes, descale, seqs, N, s);
+  return x_dtype == 1 ? launch_blocks_impl<128, __nv_bfloat16>(x, rotate, block_rows, codes, descale, seqs, N, s)
+                      : launch_blocks_impl<128, float>(x, rotate, block_rows, codes, descale, seqs, N, s);
+}
 
 fa_status launch_fp8_quantize(const void* x, int x_dtype, int rotate, void* codes, float* descale, long long rows,
                               int d, cudaStream_t s) {

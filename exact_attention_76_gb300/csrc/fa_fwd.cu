@@ -121,6 +121,7 @@ struct FwdSmem {
   uint64_t o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
+  float vmax_part[2][4];
   CtaAbort abort;
 };
 
@@ -137,10 +138,11 @@ __device__ __forceinline__ void issue_mma_ts(bool fp8, uint32_t d, uint32_t a, u
 // P for one row of a key block: p_i = 2^(s_i * c - m), packed into the words
 // written to TMEM (bf16 pairs, or four e4m3); returns the sum of the p_i.  The
 // scores s are left unchanged.  EMU of the kBN / 4 groups of four use the
-// polynomial exp2 (spread evenly), the rest ex2.approx.
-template <bool FP8, int EMU, int DEG>
+// polynomial exp2 (spread evenly), the rest ex2.approx.  With PMUL the e4m3
+// words hold p_i * pmul (the block-quantised V's relative scale).
+template <bool FP8, int EMU, int DEG, bool PMUL = false>
 __device__ __forceinline__ float exp2_pack_row(const float (&s)[kBN], float c, float m,
-                                               uint32_t (&pw)[FP8 ? kBN / 4 : kBN / 2]) {
+                                               uint32_t (&pw)[FP8 ? kBN / 4 : kBN / 2], float pmul = 1.0f) {
   const float2 c2 = make_float2(c, c);
   const float2 nm2 = make_float2(-m, -m);
   float2 part0 = make_float2(0.f, 0.f), part1 = make_float2(0.f, 0.f);
@@ -159,7 +161,11 @@ __device__ __forceinline__ float exp2_pack_row(const float (&s)[kBN], float c, f
     }
     part0 = __fadd2_rn(part0, y0);
     part1 = __fadd2_rn(part1, y1);
-    if constexpr (FP8) {
+    if constexpr (FP8 && PMUL) {  // the operand carries a factor, the sum does not
+      const float2 z0 = __fmul2_rn(y0, make_float2(pmul, pmul));
+      const float2 z1 = __fmul2_rn(y1, make_float2(pmul, pmul));
+      pw[g] = pack_e4m3x4(z0.x, z0.y, z1.x, z1.y);
+    } else if constexpr (FP8) {
       pw[g] = pack_e4m3x4(y0.x, y0.y, y1.x, y1.y);
     } else {
       pw[2 * g] = pack_bf16x2(y0.x, y0.y);
@@ -169,7 +175,9 @@ __device__ __forceinline__ float exp2_pack_row(const float (&s)[kBN], float c, f
   return (part0.x + part0.y) + (part1.x + part1.y);
 }
 
-template <int D, bool FP8>
+// BS: block-quantised e4m3 inputs (one scale per 128 query rows and per 64
+// keys, of Q and of K and V), FP8 only.
+template <int D, bool FP8, bool BS>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
@@ -371,9 +379,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = n_t[t];
     float c = scale_log2;
     float o_mult = 1.0f;
-    if (FP8) {
+    if constexpr (FP8 && !BS) {
       c = scale_log2 * __ldg(descale_q) * __ldg(descale_k);
       o_mult = __ldg(descale_v);
+    }
+    // Block scales ("FLASH-ATTN", FlashAttention-3 > Low-precision with FP8,
+    // block quantisation): S of query block t and key block j is scaled by
+    // delta_q(t) delta_k(j); V's block scale delta_v(j) goes into P's e4m3
+    // operand relative to the head's largest one, which O takes at the end.
+    float cq = 0.f, inv_vmax = 1.f, dk_cur = 0.f, dv_cur = 0.f;
+    const float* dk_row = nullptr;
+    const float* dv_row = nullptr;
+    if constexpr (BS) {
+      dk_row = descale_k + static_cast<size_t>(bh_kv) * n_kv_all;
+      dv_row = descale_v + static_cast<size_t>(bh_kv) * n_kv_all;
+      if (nt > 0) {  // uniform over the warpgroup
+        cq = scale_log2 * __ldg(descale_q + static_cast<size_t>(bh) * ((N + kBM - 1) / kBM) + q0 / kBM + t);
+        float vm = 0.f;
+        for (int jj = r; jj < n_kv_all; jj += kBM) vm = fmaxf(vm, __ldg(dv_row + jj));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
+        if ((r & 31) == 0) sh.vmax_part[t][warp & 3] = vm;
+        named_bar_sync(1 + t, kBM);
+        vm = fmaxf(fmaxf(sh.vmax_part[t][0], sh.vmax_part[t][1]), fmaxf(sh.vmax_part[t][2], sh.vmax_part[t][3]));
+        o_mult = vm > 0.f ? vm : 1.0f;
+        inv_vmax = 1.0f / o_mult;
+        dk_cur = __ldg(dk_row);
+        dv_cur = __ldg(dv_row);
+      }
     }
     float m_used = -INFINITY;
     float l_sum = 0.0f;
@@ -405,6 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int j = 0; j < nt; ++j) {
+      float pmul = 1.0f, dk_nx = 0.f, dv_nx = 0.f;
+      if constexpr (BS) {
+        c = cq * dk_cur;
+        pmul = dv_cur * inv_vmax;
+        if (j + 1 < nt) {  // next block's scales, loaded a block ahead
+          dk_nx = __ldg(dk_row + j + 1);
+          dv_nx = __ldg(dv_row + j + 1);
+        }
+      }
       ok = mbar_wait<true>(&sh.s_full[t], j & 1, &sh.abort, &g_err_fwd);
       if (!ok) break;
       tc_fence_after();
@@ -464,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_cand;
         }
         // masked blocks use ex2 throughout, so masked P is exactly 0
-        row_sum = exp2_pack_row<FP8, 0, C::kPolyDeg>(s, c, m_used + C::kPShiftLog2, pw);
+        row_sum = exp2_pack_row<FP8, 0, C::kPolyDeg, BS>(s, c, m_used + C::kPShiftLog2, pw, pmul);
       }
       l_sum = l_sum * alpha + row_sum;
       // PV_t(j-1) must be complete before P_t(j) overwrites P_t(j-1) and before
@@ -490,6 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sh.p_full[t]);
+      if constexpr (BS) {
+        dk_cur = dk_nx;
+        dv_cur = dv_nx;
+      }
     }
     // Epilogue: O = O~ / l in bf16, staged with the 128-byte swizzle in this
     // tile's own Q space and written by TMA stores, which drop box rows past N.
@@ -555,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool BS>
 fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D, FP8>;
   const int BH = a.B * a.H;
@@ -566,7 +612,7 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
       !encode_rows_map(&mk, a.k, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN) ||
       !encode_rows_map(&mv, a.v, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN))
     return FA_ERR_LAUNCH;
-  auto kern = fa_fwd_kernel<D, FP8>;
+  auto kern = fa_fwd_kernel<D, FP8, BS>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FA_ERR_LAUNCH;
   dim3 grid(static_cast<unsigned>(((a.N + 2 * kBM - 1) / (2 * kBM)) * BH));
@@ -580,10 +626,16 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_fwd_impl<64, false>(a, stream) : launch_fwd_impl<128, false>(a, stream);
+  return a.d == 64 ? launch_fwd_impl<64, false, false>(a, stream) : launch_fwd_impl<128, false, false>(a, stream);
 }
 
-fa_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) { return launch_fwd_impl<128, true>(a, stream); }
+fa_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
+  return launch_fwd_impl<128, true, false>(a, stream);
+}
+
+fa_status launch_fwd_fp8_blocks(const FwdArgs& a, cudaStream_t stream) {
+  return launch_fwd_impl<128, true, true>(a, stream);
+}
 
 uint32_t fwd_bf16_take_error(cudaStream_t s) {
   uint32_t v = 0, zero = 0;

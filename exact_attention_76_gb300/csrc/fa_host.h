@@ -23,7 +23,7 @@ struct FwdArgs {
   const void* v;
   void* o;
   float* lse;
-  const float* descale_q;  // FP8 only (device pointers)
+  const float* descale_q;  // FP8 only (device pointers): one value, or one per block
   const float* descale_k;
   const float* descale_v;
   int B, H, N, d;
@@ -58,6 +58,9 @@ fa_status launch_bwd_dq_convert(const float* dq_acc, void* dq, long long rows, i
 fa_status launch_timeout_probe(unsigned int limit_us, cudaStream_t stream);
 fa_status launch_fp8_quantize(const void* x, int x_dtype, int rotate, void* codes, float* descale, long long rows,
                               int d, cudaStream_t stream);
+fa_status launch_fp8_quantize_blocks(const void* x, int x_dtype, int rotate, int block_rows, void* codes,
+                                     float* descale, int seqs, int N, int d, cudaStream_t stream);
+fa_status launch_fwd_fp8_blocks(const FwdArgs& a, cudaStream_t stream);
 
 // Reads and clears each translation unit's device error word (stream-ordered
 // copy followed by a stream synchronisation done by the caller).

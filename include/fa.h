@@ -170,6 +170,51 @@ fa_status fa_fp8_quantize(const void* x, int x_dtype, int hadamard, void* codes,
                           int d, void* stream);
 
 /*
+ * Block sizes of the block-quantised FP8 path: one scale per 128 rows of Q
+ * (the forward's query tile, B_r) and per 64 rows of K and of V (its key
+ * block, B_c).
+ */
+#define FA_FP8_BLOCK_Q 128
+#define FA_FP8_BLOCK_KV 64
+
+/*
+ * FP8 forward on block-quantised inputs ("FLASH-ATTN", FlashAttention-3 >
+ * Low-precision with FP8, block quantisation: Q, K and V are cut into blocks
+ * of B_r x d or B_c x d rows quantised each with its own scale; the kernel,
+ * which works block by block, scales each block of S by the scales of its Q
+ * and K blocks).
+ *   q8, k8, v8 : [B,H,N,d] e4m3 codes, d = 128.
+ *   descale_q  : DEVICE [B*H, ceil(N/128)] fp32, the scale of rows
+ *                [128 b, 128 b + 128) of each head of Q.
+ *   descale_k, descale_v : DEVICE [B*H, ceil(N/64)] fp32, per 64 rows of K
+ *                and of V.  All scales positive and finite.
+ *   o, lse, B, H, N, causal, scale, stream : as fa_fwd_fp8.
+ * S for query block i and key block j is scale * dq_i dk_j q8 k8^T.  V's
+ * block scale is applied to P's e4m3 operand relative to the largest V scale
+ * of the head (P * 2^8 * dv_j / max dv, never above 448), and O is multiplied
+ * by that largest scale at the end.
+ */
+fa_status fa_fwd_fp8_blocks(const void* q8, const void* k8, const void* v8, const float* descale_q,
+                            const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H,
+                            int N, int d, int causal, float scale, void* stream);
+
+/*
+ * Block e4m3 storage for fa_fwd_fp8_blocks (block quantisation of the same
+ * section; optional Hadamard rotation as in fa_fp8_quantize).
+ *   x          : [seqs, N, d] input, fp32 (x_dtype = 0) or bf16 (x_dtype = 1),
+ *                device.
+ *   block_rows : rows per block, 1..1024 (FA_FP8_BLOCK_Q for Q,
+ *                FA_FP8_BLOCK_KV for K and V); the last block of a sequence
+ *                holds the remaining N mod block_rows rows, if any.
+ *   codes      : [seqs, N, d] e4m3 codes out, device.
+ *   descale    : [seqs, ceil(N / block_rows)] fp32 out, device: per block
+ *                delta = max|y| / 448 (1 if the block is all zero).
+ *   d in {64, 128}; seqs in 1..65535; N >= 1.  One launch on `stream`.
+ */
+fa_status fa_fp8_quantize_blocks(const void* x, int x_dtype, int hadamard, int block_rows, void* codes,
+                                 float* descale, int seqs, int N, int d, void* stream);
+
+/*
  * fa_bwd without a workspace argument, for callers that cannot allocate
  * device memory: a plugin inside another runtime that is handed only its
  * input and output tensors, or code on a path where cudaMalloc (which can

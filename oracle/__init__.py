@@ -15,6 +15,8 @@ from .attention import (  # noqa: F401
     forward_fp8_reference,
     forward_gqa,
     hadamard_matrix,
+    dequantize_e4m3_blocks,
+    quantize_e4m3_blocks_reference,
     quantize_e4m3_reference,
     rotate_rows,
     head_backward,

@@ -287,6 +287,43 @@ def quantize_e4m3_reference(x):
     return y.to(torch.float8_e4m3fn).view(torch.uint8).numpy(), delta
 
 
+def quantize_e4m3_blocks_reference(x, block_rows: int):
+    """Block e4m3 storage ("FLASH-ATTN", FlashAttention-3 > Low-precision with
+    FP8, block quantisation: Q, K and V are cut into blocks of B_r x d or
+    B_c x d rows and each block is quantised on its own, with one scale).
+
+    x is [..., N, d]; every leading index is one sequence, and the blocks are
+    rows [b*block_rows, (b+1)*block_rows) of a sequence (the last one may be
+    shorter).  Per block: delta = amax|x| / 448 (1 for an all-zero block) and
+    code = e4m3_rne(x / delta), the rounding being torch's float8_e4m3fn
+    conversion of the float32 value of x / delta.  Returns (codes as uint8 with
+    the shape of x, deltas [..., ceil(N / block_rows)] float64)."""
+    import torch
+    x = _f64(x)
+    N = x.shape[-2]
+    nb = -(-N // block_rows)
+    codes = np.empty(x.shape, dtype=np.uint8)
+    deltas = np.empty(x.shape[:-2] + (nb,), dtype=np.float64)
+    for b in range(nb):
+        rows = slice(b * block_rows, min(N, (b + 1) * block_rows))
+        blk = x[..., rows, :]
+        amax = np.abs(blk).max(axis=(-2, -1))
+        delta = np.where(amax > 0, amax / 448.0, 1.0)
+        y = np.clip(blk / delta[..., None, None], -448.0, 448.0)
+        codes[..., rows, :] = torch.from_numpy(y).to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        deltas[..., b] = delta
+    return codes, deltas
+
+
+def dequantize_e4m3_blocks(codes, deltas, block_rows: int):
+    """x ~= delta_block * e4m3(code): the inverse mapping of the block storage
+    above (float64)."""
+    import torch
+    c = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    scale = np.repeat(_f64(deltas), block_rows, axis=-1)[..., : c.shape[-2]]
+    return c * scale[..., None]
+
+
 # ---------------------------------------------------------------------------
 # Grouped-query attention.
 # ---------------------------------------------------------------------------

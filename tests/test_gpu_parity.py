@@ -260,6 +260,81 @@ def test_fp8_forward_with_incoherent_processing(causal, N):
     assert e <= FP8_O_REL_FRO, f"FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
 
 
+# ---------------------------------------------------------------- FP8, block quantisation
+
+@pytest.mark.parametrize("hadamard", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("block_rows", [64, 128])
+def test_fp8_quantize_blocks_matches_reference(hadamard, d, block_rows):
+    # Same decision rule as the per-tensor quantiser: codes may differ only where
+    # y/delta lies within 2e-6 (relative) of an e4m3 rounding boundary.
+    x = inputs.draw_outlier_fp32(1, 3, 300, d, seed=8)[0]
+    x = x * torch.exp2(torch.arange(300, dtype=torch.float32) // 50 - 3.0)[None, None, :, None]
+    codes, dsc = api.fa_fp8_quantize_blocks(x.cuda(), hadamard, block_rows)
+    torch.cuda.synchronize()
+    y = oracle.rotate_rows(x) if hadamard else f64(x)
+    ref_codes, ref_deltas = oracle.quantize_e4m3_blocks_reference(y, block_rows)
+    got_d = dsc.cpu().numpy().astype(np.float64).reshape(ref_deltas.shape)
+    np.testing.assert_allclose(got_d, ref_deltas, rtol=1e-6, atol=0)
+    got = codes.cpu().numpy()
+    t = y / np.repeat(ref_deltas, block_rows, axis=-1)[..., :300, None]
+    ok = (got == ref_codes) | (got == _e4m3_codes(t * (1 - 2e-6))) | (got == _e4m3_codes(t * (1 + 2e-6)))
+    assert ok.all()
+    assert (got == ref_codes).mean() > 0.999
+
+
+def _block_scaled_inputs(B, H, N, d, seed):
+    # outlier inputs whose 64-row blocks also differ in magnitude by up to 2^12
+    q, k, v = inputs.draw_outlier_fp32(B, H, N, d, seed=seed)
+    g = torch.Generator().manual_seed(seed + 100)
+    out = []
+    for t in (q, k, v):
+        e = torch.randint(-12, 1, (B, H, -(-N // 64)), generator=g).to(torch.float32)
+        f = torch.exp2(e).repeat_interleave(64, dim=-1)[..., :N, None]
+        out.append(t * f if t is v else t * f.sqrt())
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [256, 1000])
+def test_fp8_blocks_forward_kernel_error(causal, N):
+    # Against exact attention on the dequantised block-quantised inputs: what
+    # remains is the kernel's own error (P as e4m3, fp32 accumulation).
+    B, H, d = 1, 2, 128
+    q, k, v = _block_scaled_inputs(B, H, N, d, seed=4)
+    scale = 1 / math.sqrt(d)
+    cq, dq = oracle.quantize_e4m3_blocks_reference(q, api.FP8_BLOCK_Q)
+    ck, dk = oracle.quantize_e4m3_blocks_reference(k, api.FP8_BLOCK_KV)
+    cv, dv = oracle.quantize_e4m3_blocks_reference(v, api.FP8_BLOCK_KV)
+    dev = [torch.from_numpy(c).cuda() for c in (cq, ck, cv)]
+    dsc = [torch.from_numpy(x.reshape(B * H, -1).astype(np.float32)).cuda() for x in (dq, dk, dv)]
+    o, lse = api.fa_fwd_fp8_blocks(*dev, *dsc, causal, scale)
+    torch.cuda.synchronize()
+    deq = [oracle.dequantize_e4m3_blocks(c, x.astype(np.float32).astype(np.float64), r)
+           for c, x, r in ((cq, dq, 128), (ck, dk, 64), (cv, dv, 64))]
+    o_ref, l_ref = oracle.forward(*deq, causal, scale)
+    e = rel_fro(f64(o), o_ref)
+    assert e <= FP8_O_REL_FRO, f"block FP8 O rel-Frobenius vs dequantised inputs {e:.3e}"
+    assert max_abs(f64(lse), l_ref) <= 2e-2
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_blocks_forward_with_incoherent_processing(causal):
+    # The whole FP8 path on the GPU: Hadamard-rotated Q and K and plain V stored
+    # per block, against exact attention on the unquantised inputs.
+    B, H, N, d = 1, 2, 1000, 128
+    q, k, v = inputs.draw_outlier_fp32(B, H, N, d, seed=4)
+    scale = 1 / math.sqrt(d)
+    q8, dsq = api.fa_fp8_quantize_blocks(q.cuda(), True, api.FP8_BLOCK_Q)
+    k8, dsk = api.fa_fp8_quantize_blocks(k.cuda(), True, api.FP8_BLOCK_KV)
+    v8, dsv = api.fa_fp8_quantize_blocks(v.cuda(), False, api.FP8_BLOCK_KV)
+    o, lse = api.fa_fwd_fp8_blocks(q8, k8, v8, dsq, dsk, dsv, causal, scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.forward_fp8_reference(q, k, v, causal, scale)
+    e = rel_fro(f64(o), o_ref)
+    assert e <= FP8_O_REL_FRO, f"block FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
+
+
 # ---------------------------------------------------------------- errors and the timeout path
 
 def test_timeout_path_reports_and_context_survives():

@@ -350,6 +350,52 @@ def test_e4m3_reference_quantiser():
     assert not np.any((codes & 0x7F) == 0x7F)
 
 
+def test_e4m3_blocks_one_block_is_the_per_tensor_quantiser():
+    x = rng(33).standard_normal((2, 3, 50, 64)) * 2.0
+    codes, deltas = oracle.quantize_e4m3_blocks_reference(x, 64)
+    assert deltas.shape == (2, 3, 1)
+    for b in range(2):
+        for h in range(3):
+            c1, d1 = oracle.quantize_e4m3_reference(x[b, h])
+            np.testing.assert_array_equal(codes[b, h], c1)
+            assert deltas[b, h, 0] == d1
+
+
+def test_e4m3_blocks_are_independent_and_scale_covariant():
+    x = rng(34).standard_normal((1, 1, 200, 128))
+    codes, deltas = oracle.quantize_e4m3_blocks_reference(x, 64)
+    assert deltas.shape == (1, 1, 4)  # 64 + 64 + 64 + 8 rows
+    y = x.copy()
+    y[..., 64:128, :] *= 2.0 ** 5  # one block scaled by a power of two
+    codes2, deltas2 = oracle.quantize_e4m3_blocks_reference(y, 64)
+    np.testing.assert_array_equal(codes2, codes)
+    np.testing.assert_array_equal(deltas2[..., [0, 2, 3]], deltas[..., [0, 2, 3]])
+    assert deltas2[0, 0, 1] == deltas[0, 0, 1] * 2.0 ** 5
+    # the largest entry of each block is stored as +-448 exactly
+    deq = oracle.dequantize_e4m3_blocks(codes, deltas, 64)
+    for b, rows in enumerate([slice(0, 64), slice(64, 128), slice(128, 192), slice(192, 200)]):
+        blk = x[..., rows, :]
+        assert abs(np.abs(deq[..., rows, :]).max() - np.abs(blk).max()) <= 1e-12 * np.abs(blk).max()
+        c = codes[..., rows, :]
+        assert np.any((c & 0x7F) == 0x7E)  # 0x7E is 448
+
+
+def test_e4m3_blocks_rounding_bound_and_zero_block():
+    x = rng(35).standard_normal((1, 2, 256, 64)) * np.exp(rng(36).standard_normal((1, 2, 256, 1)) * 3)
+    x[0, 1, 128:192] = 0.0
+    codes, deltas = oracle.quantize_e4m3_blocks_reference(x, 64)
+    assert deltas[0, 1, 2] == 1.0 and not np.any(codes[0, 1, 128:192])
+    deq = oracle.dequantize_e4m3_blocks(codes, deltas, 64)
+    dl = np.repeat(deltas, 64, axis=-1)[..., None]
+    normal = np.abs(x) >= 2.0 ** -6 * dl
+    # normals: half an ulp of a 3-bit mantissa; subnormals: half the spacing 2^-9 delta
+    assert np.all(np.abs(deq - x)[normal] <= 2.0 ** -4 * np.abs(x)[normal] * (1 + 1e-12))
+    assert np.all(np.abs(deq - x)[~normal] <= (2.0 ** -10 * dl * np.ones_like(x))[~normal] * (1 + 1e-12))
+    # block scales follow the local magnitude
+    amax = np.abs(x.reshape(1, 2, 4, 64, 64)).max(axis=(-2, -1))
+    np.testing.assert_allclose(deltas, np.where(amax > 0, amax / 448.0, 1.0), rtol=1e-15)
+
+
 # ---------------------------------------------------------------- grouped-query attention
 
 def test_gqa_with_one_query_head_per_kv_head_is_plain_attention():
