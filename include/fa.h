@@ -192,7 +192,9 @@ fa_status fa_fp8_quantize(const void* x, int x_dtype, int hadamard, void* codes,
  * S for query block i and key block j is scale * dq_i dk_j q8 k8^T.  V's
  * block scale is applied to P's e4m3 operand relative to the largest V scale
  * of the head (P * 2^8 * dv_j / max dv, never above 448), and O is multiplied
- * by that largest scale at the end.
+ * by that largest scale at the end.  Where V's block scales differ, small P
+ * values lose e4m3 precision; passing one V scale per head (the same value in
+ * every block of descale_v) avoids that.
  */
 fa_status fa_fwd_fp8_blocks(const void* q8, const void* k8, const void* v8, const float* descale_q,
                             const float* descale_k, const float* descale_v, void* o, float* lse, int B, int H,
