@@ -246,6 +246,33 @@ def fa_fp8_quantize_blocks(x, hadamard: bool, block_rows: int, codes=None, desca
     return codes, descale
 
 
+def fa_decode_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
+    return int(_lib.load().fa_decode_workspace_size(B, H, Hkv, N, d))
+
+
+def fa_decode(q, k, v, scale: float, o=None, lse=None, workspace=None, stream=None):
+    """One query row per (batch, head) against the key/value cache k, v
+    [B, Hkv, N, d]; q is [B, H, d] bf16.  Returns bf16 O [B, H, d] and fp32 L
+    [B, H]."""
+    lib = _lib.load()
+    B, H, d = q.shape
+    _, Hkv, N, _ = k.shape
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16, (B, Hkv, N, d))
+    _check(v, "v", torch.bfloat16, (B, Hkv, N, d))
+    o = torch.empty((B, H, d), dtype=torch.bfloat16, device=q.device) if o is None else o
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "o", torch.bfloat16, (B, H, d))
+    _check(lse, "lse", torch.float32, (B, H))
+    ws_bytes = fa_decode_workspace_size(B, H, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8)
+    _lib.check("fa_decode", lib.fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                          workspace.numel(), B, H, Hkv, N, d, float(scale), _stream_ptr(stream)))
+    return o, lse
+
+
 def fa_status_string(status: int) -> str:
     return _lib.load().fa_status_string(int(status)).decode()
 

@@ -260,6 +260,28 @@ fa_status fa_fp8_quantize_blocks(const void* x, int x_dtype, int hadamard, int b
                                     static_cast<cudaStream_t>(stream));
 }
 
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int N, int d) {
+  if (B <= 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  return round16(decode_workspace_bytes(B, H, Hkv, N, d));
+}
+
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                    size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(q, k, v, o, lse)) != FA_OK) return st;
+  if (B <= 0 || H <= 0 || N <= 0 || Hkv <= 0 || H % Hkv != 0 || H / Hkv > 16 || B > 65535 ||
+      static_cast<long long>(B) * Hkv > 65535)
+    return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (workspace == nullptr || workspace_bytes < fa_decode_workspace_size(B, H, Hkv, N, d))
+    return FA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return FA_ERR_ALIGNMENT;
+  if ((st = check_device()) != FA_OK) return st;
+  DecodeArgs a{q, k, v, o, lse, static_cast<float*>(workspace), B, H, Hkv, N, d, scale};
+  return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
 fa_status fa_fp8_quantize(const void* x, int x_dtype, int hadamard, void* codes, float* descale, long long rows,
                           int d, void* stream) {
   fa_status st;
@@ -287,7 +309,7 @@ const char* fa_status_string(fa_status s) {
 fa_status fa_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_LAUNCH;
-  uint32_t e = fwd_bf16_take_error(s) | bwd_take_error(s) | probe_take_error(s);
+  uint32_t e = fwd_bf16_take_error(s) | bwd_take_error(s) | probe_take_error(s) | decode_take_error(s);
   if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_LAUNCH;
   if (e & FA_DEVERR_TIMEOUT) return FA_ERR_TIMEOUT;
   if (e != 0) return FA_ERR_LAUNCH;

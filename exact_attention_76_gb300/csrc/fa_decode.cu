@@ -1,0 +1,399 @@
+// Decode attention for sm_103a: one query row per (batch, query head) against
+// a long key/value cache, the step that generates one token ("FlashAttention
+// 三代演进", the decode case -- batch of short queries, memory-bound, tiled
+// differently from the forward over whole sequences; the row it computes is the
+// standard attention of "FLASH-ATTN", FlashAttention-2 > Background).
+//
+// The work is reading K and V once, so the kernel is organised for HBM
+// bandwidth, not for the tensor cores:
+//  * the keys of one key/value head are cut into chunks; one CTA takes one
+//    chunk for all the query heads that share that key/value head (grouped
+//    queries read the cache once), and enough chunks exist to fill the GPU;
+//  * a TMA warp streams the chunk's K tiles, then its V tiles (64 keys each,
+//    128-byte swizzle) through a 3-slot ring guarded by full/empty mbarriers;
+//    three CTAs share an SM;
+//  * pass 1: 4 threads per key compute the scaled scores q_h . k (in log2
+//    units) of every query head, packed fp32x2 FMAs, into shared memory;
+//  * per head, the chunk's maximum m and sum l of 2^(s - m), with s replaced
+//    by p = 2^(s - m) in place;
+//  * pass 2: each thread owns two output columns for a quarter of the keys and
+//    accumulates sum p v for every head; the quarters are summed at the end;
+//  * the chunk's (m, l, unnormalised O) go to a workspace, and a second kernel
+//    merges the chunks of a row with the block-merge rule of "FLASH-ATTN",
+//    FlashAttention > Tiling and Recomputation: m = max m_c,
+//    l = sum l_c 2^(m_c - m), O = sum O_c 2^(m_c - m) / l, L = m ln 2 + ln l.
+#include <cuda_bf16.h>
+
+#include "fa_common.cuh"
+#include "fa_host.h"
+
+namespace fa {
+
+namespace {
+
+__device__ uint32_t g_err_dec;
+
+constexpr int kDecCompute = 256;           // 8 compute warps
+constexpr int kDecThreads = kDecCompute + 32;  // + the TMA warp
+constexpr int kDecTile = 64;               // keys per K or V tile
+constexpr int kDecSlots = 3;
+constexpr int kDecScoreBytes = 16384;      // chunk keys x padded heads x 4 bytes
+
+template <int D>
+struct DecCfg {
+  static constexpr int kColBlocks = D * 2 / 128;        // 128-byte column blocks of a row
+  static constexpr int kBlockBytes = kDecTile * 128;    // one column block of a tile
+  static constexpr int kTileBytes = kDecTile * D * 2;   // one K or V tile
+  static constexpr int kQuarter = D / 4;                // elements of a row per score thread
+  static constexpr int kQStride = kQuarter + 4;         // padded fp32 quarter row of q
+  static constexpr int kPairs = D / 2;                  // column pairs (pass 2)
+  static constexpr int kGroups = kDecCompute / kPairs;  // key groups (pass 2)
+  static constexpr int kKeysPerGroup = kDecTile / kGroups;
+  static_assert(D == 64 || D == 128, "head dim");
+  // The ring also holds the key-group sums at the end ([kGroups][g][D] fp32).
+  __host__ __device__ static constexpr int ring_bytes(int g4) {
+    return kDecSlots * kTileBytes > kGroups * g4 * D * 4 ? kDecSlots * kTileBytes : kGroups * g4 * D * 4;
+  }
+};
+
+struct DecSmem {
+  uint64_t full[kDecSlots];
+  uint64_t empty[kDecSlots];
+  float m[16];
+  float l[16];
+  CtaAbort abort;
+};
+
+// Byte offset of element (row r, column e) of a tile stored as column blocks of
+// 64 rows x 128 bytes with the 128-byte swizzle (16-byte chunk c of row r at
+// chunk c ^ (r & 7)).
+__device__ __forceinline__ int swz_off(int r, int e) {
+  const int cb = e >> 6;
+  const int c = (e & 63) >> 3;
+  return cb * (kDecTile * 128) + r * 128 + (((c ^ (r & 7)) << 4) | ((e & 7) << 1));
+}
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// grid (nsplit, B*Hkv); each CTA: keys [chunk*C, min(N, chunk*C + C)) of one
+// key/value head, for its g query heads.  G: g fixed at compile time (1, 2, 4,
+// 8), or 16 for any g up to 16 read at run time.
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads, 3)
+    fa_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                     const __nv_bfloat16* __restrict__ q, float* __restrict__ part, int H, int Hkv, int N, int C,
+                     int nsplit, float scale_log2) {
+  using Cf = DecCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ DecSmem sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int G4 = (G + 3) & ~3;
+  uint8_t* s_ring = smem;                                         // kDecSlots tiles
+  float* s_score = reinterpret_cast<float*>(smem + Cf::ring_bytes(G4));  // [C][gp]
+  float* s_q = s_score + kDecScoreBytes / 4;                      // [g][4][kQStride]
+
+  if (*reinterpret_cast<volatile uint32_t*>(&g_err_dec) & FA_DEVERR_TIMEOUT) return;
+  const int g = G < 16 ? G : H / Hkv;
+  const int gp = (g + 3) & ~3;
+  const int chunk = static_cast<int>(blockIdx.x);
+  const int bkv = static_cast<int>(blockIdx.y);  // b * Hkv + kv head
+  const int key_begin = chunk * C;
+  const int key_end = min(N, key_begin + C);
+  const int n_tiles = (key_end - key_begin + kDecTile - 1) / kDecTile;
+  const int bq0 = (bkv / Hkv) * H + (bkv % Hkv) * g;  // first query row (b * H + h)
+  const int warp = static_cast<int>(warp_id());
+
+  if (threadIdx.x == 0) {
+    sh.abort.flag = 0;
+    for (int s = 0; s < kDecSlots; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], kDecCompute / 32);
+    }
+    fence_barrier_init();
+  }
+  // q of the group, fp32, times scale * log2 e, each quarter row padded so that
+  // the four quarters fall in different banks.
+  for (int i = threadIdx.x; i < g * D; i += kDecThreads) {
+    const int h = i / D, e = i % D;
+    s_q[(h * 4 + e / Cf::kQuarter) * Cf::kQStride + e % Cf::kQuarter] =
+        __bfloat162float(q[static_cast<size_t>(bq0 + h) * D + e]) * scale_log2;
+  }
+  __syncthreads();
+
+  if (warp == kDecCompute / 32) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      int issued = 0;
+      for (int it = 0; it < 2 * n_tiles && !sh.abort.flag; ++it) {
+        const int slot = issued % kDecSlots;
+        const int round = issued / kDecSlots;
+        if (round > 0 && !mbar_wait<true>(&sh.empty[slot], (round - 1) & 1, &sh.abort, &g_err_dec)) break;
+        const bool is_k = it < n_tiles;
+        const int key0 = key_begin + (is_k ? it : it - n_tiles) * kDecTile;
+        mbar_arrive_expect_tx(&sh.full[slot], Cf::kTileBytes);
+        for (int cb = 0; cb < Cf::kColBlocks; ++cb)
+          tma_load_3d(s_ring + slot * Cf::kTileBytes + cb * Cf::kBlockBytes, is_k ? &map_k : &map_v, cb * 64, key0,
+                      bkv, &sh.full[slot]);
+        ++issued;
+      }
+      if (sh.abort.flag) {
+        for (int s = 0; s < kDecSlots && s < issued; ++s) {
+          const int last = s + ((issued - 1 - s) / kDecSlots) * kDecSlots;
+          mbar_wait_drain(&sh.full[s], (last / kDecSlots) & 1, &g_err_dec);
+        }
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ---------------------------------------------------------------- compute
+  const int t = threadIdx.x;
+  bool ok = true;
+  int used = 0;  // ring uses so far
+  auto acquire = [&](int slot) {  // warp-uniform result: the warp shuffles after it
+    const bool got = ok && mbar_wait<true>(&sh.full[slot], (used / kDecSlots) & 1, &sh.abort, &g_err_dec);
+    ok = __all_sync(0xffffffffu, got);
+    return ok;
+  };
+  auto release = [&](int slot) {
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive(&sh.empty[slot]);
+    ++used;
+  };
+
+  // Pass 1: scores.  Thread t: key k = t / 4 of the tile, quarter p = t % 4.
+  {
+    const int k = t >> 2, p = t & 3;
+    const float* qp = s_q + p * Cf::kQStride;
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      const int slot = used % kDecSlots;
+      if (!acquire(slot)) break;
+      const uint8_t* kt = s_ring + slot * Cf::kTileBytes;
+      float2 acc[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[h] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < Cf::kQuarter / 8; ++c) {  // 16-byte chunks of the quarter
+        const uint4 w = *reinterpret_cast<const uint4*>(kt + swz_off(k, p * Cf::kQuarter + c * 8));
+        const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+        const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          if (h < g) {
+            const float4 qa = *reinterpret_cast<const float4*>(qp + h * 4 * Cf::kQStride + c * 8);
+            const float4 qb = *reinterpret_cast<const float4*>(qp + h * 4 * Cf::kQStride + c * 8 + 4);
+            acc[h] = __ffma2_rn(k0, make_float2(qa.x, qa.y), acc[h]);
+            acc[h] = __ffma2_rn(k1, make_float2(qa.z, qa.w), acc[h]);
+            acc[h] = __ffma2_rn(k2, make_float2(qb.x, qb.y), acc[h]);
+            acc[h] = __ffma2_rn(k3, make_float2(qb.z, qb.w), acc[h]);
+          }
+        }
+      }
+      release(slot);
+      const int key = tile * kDecTile + k;  // within the chunk
+      const bool valid = key_begin + key < key_end;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (h < g) {
+          float v = acc[h].x + acc[h].y;
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          if ((h & 3) == p) s_score[key * gp + h] = valid ? v : -INFINITY;
+        }
+      }
+    }
+  }
+  named_bar_sync(1, kDecCompute);
+
+  // Per head: m = max over the chunk, p = 2^(s - m) in place, l = sum p.
+  const int n_keys = n_tiles * kDecTile;
+  for (int h = warp; h < g; h += kDecCompute / 32) {
+    float m = -INFINITY;
+    for (int key = lane_id(); key < n_keys; key += 32) m = fmaxf(m, s_score[key * gp + h]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float l = 0.f;
+    for (int key = lane_id(); key < n_keys; key += 32) {
+      const float pv = ex2_approx(s_score[key * gp + h] - m);
+      s_score[key * gp + h] = pv;
+      l += pv;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    if (lane_id() == 0) {
+      sh.m[h] = m;
+      sh.l[h] = l;
+    }
+  }
+  named_bar_sync(1, kDecCompute);
+
+  // Pass 2: O_h += sum_k p_hk v_k.  Thread t: column pair cp, key group kg.
+  const int cp = t % Cf::kPairs, kg = t / Cf::kPairs;
+  float2 o[G4];
+#pragma unroll
+  for (int h = 0; h < G4; ++h) o[h] = make_float2(0.f, 0.f);
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    const int slot = used % kDecSlots;
+    if (!acquire(slot)) break;
+    const uint8_t* vt = s_ring + slot * Cf::kTileBytes;
+#pragma unroll
+    for (int kk = 0; kk < Cf::kKeysPerGroup; ++kk) {
+      const int k = kg * Cf::kKeysPerGroup + kk;
+      const float2 v = bf16x2_to_float2(*reinterpret_cast<const uint32_t*>(vt + swz_off(k, 2 * cp)));
+      const float* pk = s_score + (tile * kDecTile + k) * gp;
+#pragma unroll
+      for (int h4 = 0; h4 < G4; h4 += 4) {
+        if (h4 < g) {
+          const float4 p4 = *reinterpret_cast<const float4*>(pk + h4);
+          o[h4] = __ffma2_rn(make_float2(p4.x, p4.x), v, o[h4]);
+          o[h4 + 1] = __ffma2_rn(make_float2(p4.y, p4.y), v, o[h4 + 1]);
+          o[h4 + 2] = __ffma2_rn(make_float2(p4.z, p4.z), v, o[h4 + 2]);
+          o[h4 + 3] = __ffma2_rn(make_float2(p4.w, p4.w), v, o[h4 + 3]);
+        }
+      }
+    }
+    release(slot);
+  }
+  // Sum the key groups through shared memory: past this barrier every issued
+  // copy has been consumed, so the ring is free.
+  const bool all_ok = named_bar_and(1, kDecCompute, ok);
+  float* red = reinterpret_cast<float*>(s_ring);  // [kGroups][g][D]
+#pragma unroll
+  for (int h = 0; h < G4; ++h)  // unrolled: o stays in registers
+    if (h < g) *reinterpret_cast<float2*>(red + (kg * g + h) * D + 2 * cp) = o[h];
+  named_bar_sync(1, kDecCompute);
+  if (all_ok) {
+    const size_t stride = D + 4;
+    for (int i = t; i < g * D; i += kDecCompute) {
+      const int h = i / D, e = i % D;
+      float s = 0.f;
+#pragma unroll
+      for (int gg = 0; gg < Cf::kGroups; ++gg) s += red[(gg * g + h) * D + e];
+      float* row = part + (static_cast<size_t>(bq0 + h) * nsplit + chunk) * stride;
+      row[e] = s;
+      if (e == 0) {
+        row[D] = sh.m[h];
+        row[D + 1] = sh.l[h];
+      }
+    }
+  }
+}
+
+// One warp per query row: merge its nsplit chunks.
+template <int D>
+__global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float* __restrict__ part,
+                                                              __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                                                              int rows, int nsplit) {
+  constexpr int E = D / 32;
+  const int row = static_cast<int>(blockIdx.x) * 8 + static_cast<int>(warp_id());
+  if (row >= rows) return;
+  const size_t stride = D + 4;
+  const float* base = part + static_cast<size_t>(row) * nsplit * stride;
+  float m = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) m = fmaxf(m, base[s * stride + D]);
+  float l = 0.f, acc[E];
+#pragma unroll
+  for (int j = 0; j < E; ++j) acc[j] = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float* r = base + s * stride;
+    const float w = ex2_approx(r[D] - m);
+    l += r[D + 1] * w;
+#pragma unroll
+    for (int j = 0; j < E; ++j) acc[j] += r[lane_id() * E + j] * w;
+  }
+  const float inv = 1.0f / l;
+#pragma unroll
+  for (int j = 0; j < E; ++j) o[static_cast<size_t>(row) * D + lane_id() * E + j] = __float2bfloat16_rn(acc[j] * inv);
+  if (lane_id() == 0) lse[row] = m * 0.69314718055994531f + logf(l);
+}
+
+template <int D, int G>
+fa_status launch_decode_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
+  using Cf = DecCfg<D>;
+  CUtensorMap mk, mv;
+  const int BHkv = a.B * a.Hkv;
+  if (!encode_rows_map(&mk, a.k, 2, D, a.N, BHkv, 64, kDecTile) ||
+      !encode_rows_map(&mv, a.v, 2, D, a.N, BHkv, 64, kDecTile))
+    return FA_ERR_LAUNCH;
+  const int g = a.H / a.Hkv;
+  const int smem = 1024 + Cf::ring_bytes((G + 3) & ~3) + kDecScoreBytes + g * 4 * Cf::kQStride * 4;
+  auto kern = fa_decode_kernel<D, G>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  const dim3 grid(static_cast<unsigned>(pl.nsplit), static_cast<unsigned>(BHkv));
+  kern<<<grid, kDecThreads, smem, s>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.q), a.part, a.H, a.Hkv, a.N,
+                                       pl.chunk, pl.nsplit, a.scale * 1.4426950408889634f);
+  const int rows = a.B * a.H;
+  fa_decode_merge_kernel<D><<<(rows + 7) / 8, 256, 0, s>>>(a.part, static_cast<__nv_bfloat16*>(a.o), a.lse, rows,
+                                                          pl.nsplit);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+DecodePlan decode_plan(int B, int H, int Hkv, int N, int d) {
+  (void)d;
+  const int g = H / Hkv;
+  const int gp = (g + 3) & ~3;
+  // chunk keys: the score buffer holds chunk x gp floats; at most 1024 keys
+  int cmax = (kDecScoreBytes / 4 / gp) / kDecTile * kDecTile;
+  if (cmax > 1024) cmax = 1024;
+  // Enough CTAs to fill 4 per SM on 152 SMs where the keys allow chunks of at
+  // least 256.
+  const long long units = static_cast<long long>(B) * Hkv;
+  long long want = (4 * 152 + units - 1) / units;
+  const long long by_min = (N + 255) / 256;
+  if (want > by_min) want = by_min;
+  long long nsplit = (N + cmax - 1) / cmax;
+  if (nsplit < want) nsplit = want;
+  if (nsplit < 1) nsplit = 1;
+  long long chunk = (N + nsplit - 1) / nsplit;
+  chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
+  DecodePlan p;
+  p.chunk = static_cast<int>(chunk);
+  p.nsplit = static_cast<int>((N + chunk - 1) / chunk);
+  return p;
+}
+
+size_t decode_workspace_bytes(int B, int H, int Hkv, int N, int d) {
+  const DecodePlan p = decode_plan(B, H, Hkv, N, d);
+  return static_cast<size_t>(B) * H * p.nsplit * (d + 4) * sizeof(float);
+}
+
+fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  const DecodePlan p = decode_plan(a.B, a.H, a.Hkv, a.N, a.d);
+  const int g = a.H / a.Hkv;
+  if (a.d == 64) {
+    switch (g) {
+      case 1: return launch_decode_impl<64, 1>(a, p, s);
+      case 2: return launch_decode_impl<64, 2>(a, p, s);
+      case 4: return launch_decode_impl<64, 4>(a, p, s);
+      case 8: return launch_decode_impl<64, 8>(a, p, s);
+      default: return launch_decode_impl<64, 16>(a, p, s);
+    }
+  }
+  switch (g) {
+    case 1: return launch_decode_impl<128, 1>(a, p, s);
+    case 2: return launch_decode_impl<128, 2>(a, p, s);
+    case 4: return launch_decode_impl<128, 4>(a, p, s);
+    case 8: return launch_decode_impl<128, 8>(a, p, s);
+    default: return launch_decode_impl<128, 16>(a, p, s);
+  }
+}
+
+uint32_t decode_take_error(cudaStream_t s) {
+  uint32_t v = 0, zero = 0;
+  cudaMemcpyFromSymbolAsync(&v, g_err_dec, sizeof(v), 0, cudaMemcpyDeviceToHost, s);
+  cudaStreamSynchronize(s);
+  cudaMemcpyToSymbolAsync(g_err_dec, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+  cudaStreamSynchronize(s);
+  return v;
+}
+
+}  // namespace fa

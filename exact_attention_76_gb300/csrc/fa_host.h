@@ -50,6 +50,27 @@ struct BwdArgs {
 
 fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);
 fa_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream);
+struct DecodeArgs {
+  const void* q;  // [B, H, d] bf16
+  const void* k;  // [B, Hkv, N, d] bf16
+  const void* v;
+  void* o;        // [B, H, d] bf16
+  float* lse;     // [B, H]
+  float* part;    // workspace: per (row, chunk) d + 4 floats
+  int B, H, Hkv, N, d;
+  float scale;
+};
+
+struct DecodePlan {
+  int chunk;   // keys per CTA (multiple of 64)
+  int nsplit;  // chunks per key/value head
+};
+
+DecodePlan decode_plan(int B, int H, int Hkv, int N, int d);
+size_t decode_workspace_bytes(int B, int H, int Hkv, int N, int d);
+fa_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
+uint32_t decode_take_error(cudaStream_t s);
+
 fa_status launch_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, long long rows, int d,
                                 cudaStream_t stream);
 fa_status launch_bwd_main(const BwdArgs& a, cudaStream_t stream);

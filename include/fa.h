@@ -217,6 +217,28 @@ fa_status fa_fp8_quantize_blocks(const void* x, int x_dtype, int hadamard, int b
                                  float* descale, int seqs, int N, int d, void* stream);
 
 /*
+ * Decode: one query row per (batch, head) against a cache of N keys and
+ * values -- the step that generates one token ("FlashAttention 三代演进": the
+ * decode case is memory-bound, a single query against all keys, and is tiled
+ * differently from the forward over whole sequences).  The row is standard
+ * attention ("FLASH-ATTN", FlashAttention-2 > Background) with no mask: the
+ * query sees every key of the cache.
+ *   q   : [B, H, d] bf16 (the new token's query rows), device.
+ *   k, v: [B, Hkv, N, d] bf16 (the cache), device; query head h reads key/value
+ *         head h / (H / Hkv); H % Hkv == 0 and H / Hkv <= 16.
+ *   o   : [B, H, d] bf16 out; lse : [B, H] fp32 out (natural-log LogSumExp of
+ *         the scaled logits).
+ *   workspace : device scratch of at least fa_decode_workspace_size(B, H,
+ *         Hkv, N, d) bytes (per-chunk partial results), caller-owned; it holds
+ *         nothing between calls.
+ *   d in {64, 128}; N >= 1.  Two launches on `stream`: the chunks, then the
+ *   merge of each row's chunks.
+ */
+size_t fa_decode_workspace_size(int B, int H, int Hkv, int N, int d);
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
+                    size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale, void* stream);
+
+/*
  * fa_bwd without a workspace argument, for callers that cannot allocate
  * device memory: a plugin inside another runtime that is handed only its
  * input and output tensors, or code on a path where cudaMalloc (which can

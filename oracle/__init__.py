@@ -9,6 +9,7 @@ from .attention import (  # noqa: F401
     LN2,
     backward,
     backward_gqa,
+    decode,
     flops_backward,
     flops_forward,
     forward,

@@ -325,6 +325,30 @@ def dequantize_e4m3_blocks(codes, deltas, block_rows: int):
 
 
 # ---------------------------------------------------------------------------
+# Decode: one query row against a key/value cache.
+# ---------------------------------------------------------------------------
+
+def decode(q, k, v, scale: float):
+    """q [B, H, d], k and v [B, Hkv, N, d] -> O [B, H, d], L [B, H] (float64).
+
+    One query row per (batch, head) attending to every key of the cache, no
+    mask: standard attention ("FLASH-ATTN", FlashAttention-2 > Background) with
+    a single query, the decode case of "FlashAttention 三代演进".  Query head h
+    reads key/value head h // (H // Hkv)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, d = q.shape
+    g = H // k.shape[1]
+    o = np.empty((B, H, v.shape[-1]))
+    lse = np.empty((B, H))
+    for b in range(B):
+        for h in range(H):
+            ob, lb, _ = head_forward(q[b, h][None, :], k[b, h // g], v[b, h // g], False, scale)
+            o[b, h] = ob[0]
+            lse[b, h] = lb[0]
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
 # Grouped-query attention.
 # ---------------------------------------------------------------------------
 

@@ -335,6 +335,73 @@ def test_fp8_blocks_forward_with_incoherent_processing(causal):
     assert e <= FP8_O_REL_FRO, f"block FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
 
 
+# ---------------------------------------------------------------- decode
+
+def _decode_case(B, H, Hkv, N, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, N, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, N, d), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 63, 64, 1000, 5000])
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (6, 2), (16, 1)])
+def test_decode_matches_oracle(d, N, H, Hkv):
+    B = 2
+    q, k, v = _decode_case(B, H, Hkv, N, d, seed=N + H)
+    scale = 1 / math.sqrt(d)
+    o, lse = api.fa_decode(q.cuda(), k.cuda(), v.cuda(), scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.decode(q, k, v, scale)
+    assert max_abs(f64(o), o_ref) <= O_MAX_ABS
+    assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
+
+
+def test_decode_long_cache_and_reused_workspace():
+    # 32768 keys per head in many chunks; the oracle's row costs O(N d), so every
+    # head is checked.  The same workspace serves two different calls.
+    B, H, Hkv, N, d = 2, 16, 4, 32768, 128
+    q, k, v = _decode_case(B, H, Hkv, N, d, seed=11)
+    scale = 1 / math.sqrt(d)
+    ws = torch.empty(api.fa_decode_workspace_size(B, H, Hkv, N, d), dtype=torch.uint8, device="cuda")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = api.fa_decode(qd, kd, vd, scale, workspace=ws)
+    o2, l2 = api.fa_decode(qd[:, :, :], kd[:, :, : N // 3].contiguous(), vd[:, :, : N // 3].contiguous(), scale,
+                           workspace=ws)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.decode(q, k, v, scale)
+    assert max_abs(f64(o1), o_ref) <= O_MAX_ABS
+    assert max_abs(f64(l1), l_ref) <= L_MAX_ABS
+    o_ref2, l_ref2 = oracle.decode(q, k[:, :, : N // 3], v[:, :, : N // 3], scale)
+    assert max_abs(f64(o2), o_ref2) <= O_MAX_ABS
+    assert max_abs(f64(l2), l_ref2) <= L_MAX_ABS
+
+
+def test_decode_equals_the_last_row_of_the_causal_forward():
+    # the same bf16 inputs through both kernels: decode of the last token against
+    # the whole cache is the forward's last causal row
+    B, H, N, d = 1, 4, 777, 128
+    q, k, v, _ = inputs.draw_bf16(B, H, N, d, seed=12)
+    scale = 1 / math.sqrt(d)
+    o_f, l_f = api.fa_fwd(q.cuda(), k.cuda(), v.cuda(), True, scale)
+    o_d, l_d = api.fa_decode(q[:, :, -1].contiguous().cuda(), k.cuda(), v.cuda(), scale)
+    torch.cuda.synchronize()
+    assert (o_d.float() - o_f[:, :, -1].float()).abs().max().item() <= 2 * O_MAX_ABS
+    assert (l_d - l_f[:, :, -1]).abs().max().item() <= 2 * L_MAX_ABS
+
+
+def test_decode_argument_checks():
+    q = torch.zeros(1, 3, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 2, 16, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(RuntimeError):
+        api.fa_decode(q, k, k, 0.1)  # 3 query heads over 2 key/value heads
+    with pytest.raises(RuntimeError):
+        api.fa_decode(torch.zeros(1, 2, 128, dtype=torch.bfloat16, device="cuda"), k, k, 0.1,
+                      workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+
+
 # ---------------------------------------------------------------- errors and the timeout path
 
 def test_timeout_path_reports_and_context_survives():

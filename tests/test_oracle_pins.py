@@ -396,6 +396,37 @@ def test_e4m3_blocks_rounding_bound_and_zero_block():
     np.testing.assert_allclose(deltas, np.where(amax > 0, amax / 448.0, 1.0), rtol=1e-15)
 
 
+# ---------------------------------------------------------------- decode
+
+def test_decode_is_the_last_row_of_causal_attention():
+    # the token at position i attends keys 0..i: row i of causal attention
+    q, k, v, _ = (t.double().numpy() for t in inputs.draw_fp32(1, 2, 40, 16, 9))
+    o_c, l_c = oracle.forward(q, k, v, True, 0.25)
+    for i in (0, 7, 39):
+        o_d, l_d = oracle.decode(q[:, :, i], k[:, :, : i + 1], v[:, :, : i + 1], 0.25)
+        np.testing.assert_allclose(o_d, o_c[:, :, i], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l_d, l_c[:, :, i], rtol=0, atol=1e-13)
+
+
+def test_decode_closed_forms_and_groups():
+    k = rng(40).standard_normal((2, 2, 33, 8))
+    v = rng(41).standard_normal((2, 2, 33, 8))
+    # q = 0: uniform weights, O = mean of V, L = ln N
+    o, lse = oracle.decode(np.zeros((2, 4, 8)), k, v, 0.5)
+    np.testing.assert_allclose(o, np.repeat(v.mean(axis=2), 2, axis=1), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, np.log(33.0), rtol=0, atol=1e-14)
+    # query heads 2h and 2h+1 share key/value head h: same query, same row
+    q = rng(42).standard_normal((2, 2, 8))
+    o, lse = oracle.decode(np.repeat(q, 2, axis=1), k, v, 0.5)
+    np.testing.assert_array_equal(o[:, 0], o[:, 1])
+    np.testing.assert_array_equal(lse[:, 2], lse[:, 3])
+    # one key dominating: O -> its value row
+    kk = k.copy()
+    kk[0, 0, 5] = 40.0 * q[0, 0] / np.linalg.norm(q[0, 0])
+    o, _ = oracle.decode(q, kk, v, 1.0)
+    np.testing.assert_allclose(o[0, 0], v[0, 0, 5], rtol=0, atol=1e-8)
+
+
 # ---------------------------------------------------------------- grouped-query attention
 
 def test_gqa_with_one_query_head_per_kv_head_is_plain_attention():
