@@ -90,6 +90,46 @@ def fa_bwd_gqa(q, k, v, o, lse, dO, causal: bool, scale: float, dq=None, dk=None
     return dq, dk, dv
 
 
+def fa_fwd_window(q, k, v, window: int, scale: float, o=None, lse=None, stream=None):
+    """Causal attention where query i sees keys i-window+1 .. i; q [B,H,N,d],
+    k and v [B,Hkv,N,d]."""
+    lib = _lib.load()
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    _check(q, "q", torch.bfloat16, (B, H, N, d))
+    for t, n in ((k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, (B, Hkv, N, d))
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "o", torch.bfloat16, (B, H, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    _lib.check("fa_fwd_window", lib.fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, N, d,
+                                                  int(window), float(scale), _stream_ptr(stream)))
+    return o, lse
+
+
+def fa_bwd_window(q, k, v, o, lse, dO, window: int, scale: float, dq=None, dk=None, dv=None, workspace=None,
+                  stream=None):
+    """Backward of fa_fwd_window; dk and dv have k's and v's shape."""
+    lib = _lib.load()
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    for t, n in ((q, "q"), (o, "o"), (dO, "dO")):
+        _check(t, n, torch.bfloat16, (B, H, N, d))
+    for t, n in ((k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, (B, Hkv, N, d))
+    _check(lse, "lse", torch.float32, (B, H, N))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=q.device)
+    _lib.check("fa_bwd_window", lib.fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                                  _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H, Hkv,
+                                                  N, d, int(window), float(scale), _stream_ptr(stream)))
+    return dq, dk, dv
+
+
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
 

@@ -130,17 +130,36 @@ using namespace fa;
 
 extern "C" {
 
-fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
-                     int d, int causal, float scale, void* stream) {
+namespace {
+
+fa_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+                     int d, int causal, int window, float scale, void* stream) {
   fa_status st;
   if ((st = check_ptrs(q, k, v, o, lse)) != FA_OK) return st;
   if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
-  if (Hkv <= 0 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (Hkv <= 0 || H % Hkv != 0 || window < 0) return FA_ERR_INVALID_ARG;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((st = check_device()) != FA_OK) return st;
-  FwdArgs a{q, k, v, o, lse, nullptr, nullptr, nullptr, B, H, N, d, causal, scale, Hkv};
+  FwdArgs a{q, k, v, o, lse, nullptr, nullptr, nullptr, B, H, N, d, causal, scale, Hkv, window};
   return launch_fwd_bf16(a, static_cast<cudaStream_t>(stream));
+}
+
+fa_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                     int N, int d, int causal, int window, float scale, void* stream);
+
+}  // namespace
+
+fa_status fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int N,
+                     int d, int causal, float scale, void* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, Hkv, N, d, causal, 0, scale, stream);
+}
+
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                        int N, int d, int window, float scale, void* stream) {
+  if (window <= 0) return FA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, H, Hkv, N, d, 1, window >= N ? 0 : window, scale, stream);
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -187,13 +206,15 @@ fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, 
                                static_cast<cudaStream_t>(stream));
 }
 
-fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+namespace {
+
+fa_status bwd_common(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
-                     int N, int d, int causal, float scale, void* stream) {
+                     int N, int d, int causal, int window, float scale, void* stream) {
   fa_status st;
   if ((st = check_ptrs(q, k, v, o, lse, dO, dq, dk, dv)) != FA_OK) return st;
   if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
-  if (Hkv <= 0 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
+  if (Hkv <= 0 || H % Hkv != 0 || window < 0) return FA_ERR_INVALID_ARG;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   const size_t need = fa_bwd_workspace_size(B, H, N, d);
@@ -205,9 +226,26 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round16(rows * sizeof(float)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = launch_bwd_preprocess(o, dO, Dvec, dq_acc, static_cast<long long>(rows), d, s)) != FA_OK) return st;
-  BwdArgs a{q, k, v, lse, dO, Dvec, dq_acc, dk, dv, B, H, N, d, causal, scale, Hkv};
+  BwdArgs a{q, k, v, lse, dO, Dvec, dq_acc, dk, dv, B, H, N, d, causal, scale, Hkv, window};
   if ((st = launch_bwd_main(a, s)) != FA_OK) return st;
   return launch_bwd_dq_convert(dq_acc, dq, static_cast<long long>(rows), d, scale, s);
+}
+
+}  // namespace
+
+fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                     int N, int d, int causal, float scale, void* stream) {
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, causal, 0, scale,
+                    stream);
+}
+
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                        int N, int d, int window, float scale, void* stream) {
+  if (window <= 0) return FA_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, 1,
+                    window >= N ? 0 : window, scale, stream);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,

@@ -168,14 +168,15 @@ __device__ __forceinline__ void bwd_item(int item, int BH, int n_blk, int group,
   bh = base_head + (r - kb * g_heads);
 }
 
-template <int D>
+// WIN: causal sliding window of `window` keys.
+template <int D, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                        const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse,
                        const float* __restrict__ dvec, __nv_bfloat16* __restrict__ dk_out,
                        __nv_bfloat16* __restrict__ dv_out, int BH, int N, int causal, float scale,
-                       float scale_log2, int head_group, int H, int qgroup) {
+                       float scale_log2, int head_group, int H, int qgroup, int window) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   static_assert(sizeof(BwdBars) <= 256, "barrier block");
@@ -201,15 +202,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hkv = H / qgroup;
   const int qh0 = (bh / hkv) * H + (bh % hkv) * qgroup;
   const int i_begin = causal ? kb : 0;
-  const int n_per = n_blk - i_begin;  // query blocks per query head
+  // With a sliding window of `window` keys (causal), the last query that sees
+  // key kb*128 + 127 is kb*128 + 126 + window.
+  const int i_end = WIN ? min(n_blk, (kb * 128 + 126 + window) / 128 + 1) : n_blk;
+  const int n_per = i_end - i_begin;  // query blocks per query head
   const int n_it = qgroup * n_per;
   // Every role walks the same (query head, query block) sequence: query
-  // blocks i_begin .. n_blk-1 of head qh0, then of qh0 + 1, and so on.
+  // blocks i_begin .. i_end-1 of head qh0, then of qh0 + 1, and so on.
   struct QCursor {
     int i, h;
   };
   auto q_advance = [&](QCursor& c, int it) {
-    if (it > 0 && ++c.i == n_blk) {
+    if (it > 0 && ++c.i == i_end) {
       c.i = i_begin;
       ++c.h;
     }
@@ -430,6 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* l2 = s_lse2 + st * 128;
       const float* dd = s_dvec + st * 128;
       const bool diag = causal && (cur.i == kb);
+      // window: query q of this block and key r are out of reach when
+      // (query - key) >= window, i.e. dq0 + q - r >= window
+      const int dq0 = (cur.i - kb) * 128;
+      const bool wblk = WIN && dq0 + 127 >= window;
       float p[128];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -449,7 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int q = cc * 32 + i + u;
-            p[q] = (diag && q < r) ? 0.f : xv[u];  // query before key: masked
+            if constexpr (WIN) p[q] = ((diag && q < r) || (wblk && dq0 + q - r >= window)) ? 0.f : xv[u];
+            else p[q] = (diag && q < r) ? 0.f : xv[u];  // query before key: masked
           }
         }
       }
@@ -610,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool WIN>
 fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const int BHq = a.B * a.H;     // query heads
@@ -621,7 +630,7 @@ fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
       !encode_rows_map(&mv, a.v, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdo, a.dO, 2, D, a.N, BHq, 64, 128) ||
       !encode_rows_map(&mdq, a.dq_acc, 4, D, a.N, BHq, 32, 128))
     return FA_ERR_LAUNCH;
-  auto kern = fa_bwd_main_kernel<D>;
+  auto kern = fa_bwd_main_kernel<D, WIN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FA_ERR_LAUNCH;
   const int n_blk = (a.N + 127) / 128;
@@ -633,7 +642,8 @@ fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   dim3 grid(static_cast<unsigned>(n_blk * BH));
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a.lse, a.D,
                                                    static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv),
-                                                   BH, a.N, a.causal, a.scale, a.scale * kLog2e, group, a.H, qgroup);
+                                                   BH, a.N, a.causal, a.scale, a.scale * kLog2e, group, a.H, qgroup,
+                                                   a.window);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -654,7 +664,9 @@ fa_status launch_bwd_preprocess(const void* o, const void* dO, float* D, float* 
 }
 
 fa_status launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_bwd_main_impl<64>(a, stream) : launch_bwd_main_impl<128>(a, stream);
+  if (a.window > 0)
+    return a.d == 64 ? launch_bwd_main_impl<64, true>(a, stream) : launch_bwd_main_impl<128, true>(a, stream);
+  return a.d == 64 ? launch_bwd_main_impl<64, false>(a, stream) : launch_bwd_main_impl<128, false>(a, stream);
 }
 
 fa_status launch_bwd_dq_convert(const float* dq_acc, void* dq, long long rows, int d, float scale,

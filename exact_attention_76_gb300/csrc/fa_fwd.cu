@@ -176,14 +176,14 @@ __device__ __forceinline__ float exp2_pack_row(const float (&s)[kBN], float c, f
 }
 
 // BS: block-quantised e4m3 inputs (one scale per 128 query rows and per 64
-// keys, of Q and of K and V), FP8 only.
-template <int D, bool FP8, bool BS>
+// keys, of Q and of K and V), FP8 only.  WIN: causal sliding window.
+template <int D, bool FP8, bool BS, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                   float* __restrict__ out_lse, const float* __restrict__ descale_q,
                   const float* __restrict__ descale_k, const float* __restrict__ descale_v, int BH, int N,
-                  int causal, float scale_log2, int H, int qgroup) {
+                  int causal, float scale_log2, int H, int qgroup, int window) {
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmem sh;
@@ -207,12 +207,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh_kv = (bh / H) * (H / qgroup) + (bh % H) / qgroup;
   const int q0 = qb * 2 * kBM;
   const int n_kv_all = (N + kBN - 1) / kBN;
-  int n_t[2];
+  // Tile t visits key blocks j_lo[t] .. n_t[t] - 1 (len[t] of them): all blocks
+  // up to the causal limit, and with a sliding window of `window` keys
+  // (window > 0, causal) none that lies entirely before the window of the
+  // tile's first row.  Tile 0's range starts first; together the two ranges
+  // cover j_begin .. n_max - 1 without a gap.
+  int n_t[2], j_lo[2], len[2];
   for (int t = 0; t < 2; ++t) {
     const int row0 = q0 + t * kBM;
-    if (row0 >= N) n_t[t] = 0;
-    else n_t[t] = causal ? min(n_kv_all, (row0 + kBM - 1) / kBN + 1) : n_kv_all;
+    if (row0 >= N) {
+      n_t[t] = 0;
+      j_lo[t] = 0;
+    } else {
+      n_t[t] = causal ? min(n_kv_all, (row0 + kBM - 1) / kBN + 1) : n_kv_all;
+      j_lo[t] = WIN ? max(0, row0 - window + 1) / kBN : 0;
+    }
+    len[t] = n_t[t] - j_lo[t];
   }
+  const int j_begin = j_lo[0];
   const int n_max = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(s_q + t * C::kQTileBytes + cb * C::kQBlockBytes, &map_q, cb * C::kBoxCols, q0 + t * kBM, bh,
                       &sh.q_full);
       int issued = 0;
-      for (int j = 0; j < n_max && !sh.abort.flag; ++j) {
+      for (int j = j_begin; j < n_max && !sh.abort.flag; ++j) {
         for (int kv = 0; kv < 2; ++kv) {  // K_j then V_j
           const int slot = issued % C::kSlots;
           const int round = issued / C::kSlots;
@@ -314,53 +326,116 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_load = [&](int idx) {
         return mbar_wait<true>(&sh.kv_full[idx % C::kSlots], (idx / C::kSlots) & 1, &sh.abort, &g_err_fwd);
       };
-      bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd) && wait_load(0);
-      if (ok) {
-        tc_fence_after();
-        // Tile 1 first: its Q may come from shared memory, while tile 0's Q is
-        // still being copied into TMEM by its warpgroup.
-        for (int t = 1; ok && t >= 0; --t) {
-          if (n_t[t] == 0) continue;
-          if (t == 0 || C::kQTm1) {
-            ok = mbar_wait<true>(&sh.q_tm[t], 0, &sh.abort, &g_err_fwd);
-            if (!ok) break;
-            tc_fence_after();
-          }
-          issue_s(t, 0);
-        }
-        if (ok) tc_commit(&sh.kv_empty[0]);
-      }
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int k_idx = 2 * j + 2;  // K_(j+1)
-        const int v_idx = 2 * j + 1;  // V_j
-        bool k_ready = false, v_ready = false;
-        for (int t = 0; ok && t < 2; ++t) {
-          // S_t(j+1): its columns are free once the warpgroup copied S_t(j) out.
-          if (j + 1 < n_t[t]) {
-            if (!k_ready) {
-              ok = wait_load(k_idx);
-              k_ready = true;
+      if constexpr (!WIN) {
+        bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd) && wait_load(0);
+        if (ok) {
+          tc_fence_after();
+          // Tile 1 first: its Q may come from shared memory, while tile 0's Q is
+          // still being copied into TMEM by its warpgroup.
+          for (int t = 1; ok && t >= 0; --t) {
+            if (n_t[t] == 0) continue;
+            if (t == 0 || C::kQTm1) {
+              ok = mbar_wait<true>(&sh.q_tm[t], 0, &sh.abort, &g_err_fwd);
+              if (!ok) break;
+              tc_fence_after();
             }
-            ok = ok && mbar_wait<true>(&sh.s_free[t], j & 1, &sh.abort, &g_err_fwd);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(t, k_idx % C::kSlots);
+            issue_s(t, 0);
           }
-          // PV_t(j) once the warpgroup wrote P_t(j).
-          if (j < n_t[t]) {
-            if (!v_ready) {
-              ok = wait_load(v_idx);
-              v_ready = true;
-            }
-            ok = ok && mbar_wait<true>(&sh.p_full[t], j & 1, &sh.abort, &g_err_fwd);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, v_idx % C::kSlots, j > 0);
-          }
+          if (ok) tc_commit(&sh.kv_empty[0]);
         }
-        if (!ok) break;
-        if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
-        if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
+        for (int j = 0; ok && j < n_max; ++j) {
+          const int k_idx = 2 * j + 2;  // K_(j+1)
+          const int v_idx = 2 * j + 1;  // V_j
+          bool k_ready = false, v_ready = false;
+          for (int t = 0; ok && t < 2; ++t) {
+            // S_t(j+1): its columns are free once the warpgroup copied S_t(j) out.
+            if (j + 1 < n_t[t]) {
+              if (!k_ready) {
+                ok = wait_load(k_idx);
+                k_ready = true;
+              }
+              ok = ok && mbar_wait<true>(&sh.s_free[t], j & 1, &sh.abort, &g_err_fwd);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(t, k_idx % C::kSlots);
+            }
+            // PV_t(j) once the warpgroup wrote P_t(j).
+            if (j < n_t[t]) {
+              if (!v_ready) {
+                ok = wait_load(v_idx);
+                v_ready = true;
+              }
+              ok = ok && mbar_wait<true>(&sh.p_full[t], j & 1, &sh.abort, &g_err_fwd);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, v_idx % C::kSlots, j > 0);
+            }
+          }
+          if (!ok) break;
+          if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
+          if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
+        }
+      } else {
+        // Load index of K_j is 2 (j - j_begin), of V_j one more (the producer's
+        // order).  Tile t's step u is key block j_lo[t] + u.
+        auto k_load = [&](int j) { return 2 * (j - j_begin); };
+        // The first S of a tile needs its Q in place: tiles whose Q sits in TMEM
+        // wait for their warpgroup's copy.
+        auto wait_q = [&](int t) {
+          if (t != 0 && !C::kQTm1) return true;
+          if (!mbar_wait<true>(&sh.q_tm[t], 0, &sh.abort, &g_err_fwd)) return false;
+          tc_fence_after();
+          return true;
+        };
+        bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd) && wait_load(k_load(j_begin));
+        if (ok) {
+          tc_fence_after();
+          // Tile 1 first: its Q may come from shared memory, while tile 0's Q is
+          // still being copied into TMEM by its warpgroup.
+  #pragma unroll
+          for (int t = 1; t >= 0; --t) {
+            if (!ok || len[t] <= 0 || j_lo[t] != j_begin) continue;
+            ok = wait_q(t);
+            if (ok) issue_s(t, k_load(j_begin) % C::kSlots);
+          }
+          if (ok) tc_commit(&sh.kv_empty[k_load(j_begin) % C::kSlots]);
+        }
+        for (int j = j_begin; ok && j < n_max; ++j) {
+          const int k_idx = k_load(j + 1);  // K_(j+1)
+          const int v_idx = k_load(j) + 1;  // V_j
+          bool k_ready = false, v_ready = false;
+  #pragma unroll
+          for (int t = 0; t < 2; ++t) {  // unrolled: the per-tile values stay in registers
+            if (!ok) break;
+            const int u = j - j_lo[t];
+            // S_t(u+1): its columns are free once the warpgroup copied S_t(u) out.
+            if (u + 1 >= 0 && u + 1 < len[t]) {
+              if (!k_ready) {
+                ok = wait_load(k_idx);
+                k_ready = true;
+              }
+              if (u >= 0) ok = ok && mbar_wait<true>(&sh.s_free[t], u & 1, &sh.abort, &g_err_fwd);
+              else ok = ok && wait_q(t);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(t, k_idx % C::kSlots);
+            }
+            // PV_t(u) once the warpgroup wrote P_t(u).
+            if (u >= 0 && u < len[t]) {
+              if (!v_ready) {
+                ok = wait_load(v_idx);
+                v_ready = true;
+              }
+              ok = ok && mbar_wait<true>(&sh.p_full[t], u & 1, &sh.abort, &g_err_fwd);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, v_idx % C::kSlots, u > 0);
+            }
+          }
+          if (!ok) break;
+          if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
+          if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
+        }
       }
       // Teardown: every MMA issued by this thread completes before TMEM is freed.
       tc_commit(&sh.drain);
@@ -376,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_col = tmem + lane_base + C::kTmP + t * 32;
     const uint32_t o_col = tmem + lane_base + C::kTmO + t * D;
     const int row_g = q0 + t * kBM + r;
-    const int nt = n_t[t];
+    const int jlo_t = t ? j_lo[1] : j_lo[0];  // first key block of this tile
+    const int nt = t ? len[1] : len[0];       // key blocks it visits
     float c = scale_log2;
     float o_mult = 1.0f;
     if constexpr (FP8 && !BS) {
@@ -404,8 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         vm = fmaxf(fmaxf(sh.vmax_part[t][0], sh.vmax_part[t][1]), fmaxf(sh.vmax_part[t][2], sh.vmax_part[t][3]));
         o_mult = vm > 0.f ? vm : 1.0f;
         inv_vmax = 1.0f / o_mult;
-        dk_cur = __ldg(dk_row);
-        dv_cur = __ldg(dv_row);
+        dk_cur = __ldg(dk_row + jlo_t);
+        dv_cur = __ldg(dv_row + jlo_t);
       }
     }
     float m_used = -INFINITY;
@@ -437,17 +513,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh.q_tm[t]);
       }
     }
-    for (int j = 0; j < nt; ++j) {
+    for (int u = 0; u < nt; ++u) {
+      const int j = jlo_t + u;  // key block
       float pmul = 1.0f, dk_nx = 0.f, dv_nx = 0.f;
       if constexpr (BS) {
         c = cq * dk_cur;
         pmul = dv_cur * inv_vmax;
-        if (j + 1 < nt) {  // next block's scales, loaded a block ahead
+        if (u + 1 < nt) {  // next block's scales, loaded a block ahead
           dk_nx = __ldg(dk_row + j + 1);
           dv_nx = __ldg(dv_row + j + 1);
         }
       }
-      ok = mbar_wait<true>(&sh.s_full[t], j & 1, &sh.abort, &g_err_fwd);
+      ok = mbar_wait<true>(&sh.s_full[t], u & 1, &sh.abort, &g_err_fwd);
       if (!ok) break;
       tc_fence_after();
       float s[kBN];
@@ -464,20 +541,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&sh.s_free[t]);  // S_t(j+1) may now be written
+      mbar_arrive(&sh.s_free[t]);  // S_t(u+1) may now be written
       const int key0 = j * kBN;
-      const bool need_mask = (causal && key0 + kBN - 1 > q0 + t * kBM) || (key0 + kBN > N);
+      // Masked entries: keys after the row (causal), past N, or before the
+      // row's window (key < row - window + 1).
+      const bool need_mask = (causal && key0 + kBN - 1 > q0 + t * kBM) || (key0 + kBN > N) ||
+                             (WIN && key0 < q0 + t * kBM + kBM - window);
       if (need_mask) {
         const int lim = causal ? min(row_g, N - 1) : N - 1;  // last visible key
+        if constexpr (WIN) {
+          const int lo = row_g - window + 1;  // first visible key
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (key0 + i > lim) s[i] = -INFINITY;
+          for (int i = 0; i < kBN; ++i)
+            if (key0 + i > lim || key0 + i < lo) s[i] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            if (key0 + i > lim) s[i] = -INFINITY;
+        }
       }
       uint32_t pw[C::kPWords];
       float row_sum;
       float alpha = 1.0f;
       bool raise = false;
-      if (C::kSpecExp && j > 0 && !need_mask) {
+      if (C::kSpecExp && u > 0 && !need_mask) {
         // Speculative: P with the current reference maximum, computed while the
         // block maximum is still being found (the two are independent); only a
         // row whose block maximum exceeds the reference by more than TAU redoes
@@ -498,21 +585,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
         const float m_cand = mx * c;
-        if (j == 0) {
+        if (u == 0) {
           m_used = m_cand;
         } else if (m_cand > m_used + C::kTauLog2) {
           raise = true;
           alpha = ex2_approx(m_used - m_cand);
           m_used = m_cand;
         }
-        // masked blocks use ex2 throughout, so masked P is exactly 0
-        row_sum = exp2_pack_row<FP8, 0, C::kPolyDeg, BS>(s, c, m_used + C::kPShiftLog2, pw, pmul);
+        // Masked blocks use ex2 throughout, so masked P is exactly 0.  A row
+        // with no visible key so far (only under a window) keeps m = -inf and
+        // takes 0 as the reference here: its p are all 0, and its first
+        // visible key raises m with alpha = 0.
+        const float m_ref = (WIN && m_used == -INFINITY) ? 0.0f : m_used;
+        row_sum = exp2_pack_row<FP8, 0, C::kPolyDeg, BS>(s, c, m_ref + C::kPShiftLog2, pw, pmul);
       }
       l_sum = l_sum * alpha + row_sum;
-      // PV_t(j-1) must be complete before P_t(j) overwrites P_t(j-1) and before
+      // PV_t(u-1) must be complete before P_t(u) overwrites P_t(u-1) and before
       // O_t is rescaled.
-      if (j > 0) {
-        ok = mbar_wait<true>(&sh.o_done[t], (j - 1) & 1, &sh.abort, &g_err_fwd);
+      if (u > 0) {
+        ok = mbar_wait<true>(&sh.o_done[t], (u - 1) & 1, &sh.abort, &g_err_fwd);
         if (!ok) break;
         tc_fence_after();
       }
@@ -601,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool FP8, bool BS>
+template <int D, bool FP8, bool BS, bool WIN>
 fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D, FP8>;
   const int BH = a.B * a.H;
@@ -612,29 +703,33 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
       !encode_rows_map(&mk, a.k, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN) ||
       !encode_rows_map(&mv, a.v, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN))
     return FA_ERR_LAUNCH;
-  auto kern = fa_fwd_kernel<D, FP8, BS>;
+  auto kern = fa_fwd_kernel<D, FP8, BS, WIN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FA_ERR_LAUNCH;
   dim3 grid(static_cast<unsigned>(((a.N + 2 * kBM - 1) / (2 * kBM)) * BH));
   const float scale_log2 = a.scale * 1.4426950408889634f;
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a.lse, a.descale_q,
                                                    a.descale_k, a.descale_v, BH, a.N, a.causal, scale_log2, a.H,
-                                                   a.H / a.Hkv);
+                                                   a.H / a.Hkv, a.window);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 }  // namespace
 
 fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
-  return a.d == 64 ? launch_fwd_impl<64, false, false>(a, stream) : launch_fwd_impl<128, false, false>(a, stream);
+  if (a.window > 0)
+    return a.d == 64 ? launch_fwd_impl<64, false, false, true>(a, stream)
+                     : launch_fwd_impl<128, false, false, true>(a, stream);
+  return a.d == 64 ? launch_fwd_impl<64, false, false, false>(a, stream)
+                   : launch_fwd_impl<128, false, false, false>(a, stream);
 }
 
 fa_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
-  return launch_fwd_impl<128, true, false>(a, stream);
+  return launch_fwd_impl<128, true, false, false>(a, stream);
 }
 
 fa_status launch_fwd_fp8_blocks(const FwdArgs& a, cudaStream_t stream) {
-  return launch_fwd_impl<128, true, true>(a, stream);
+  return launch_fwd_impl<128, true, true, false>(a, stream);
 }
 
 uint32_t fwd_bf16_take_error(cudaStream_t s) {

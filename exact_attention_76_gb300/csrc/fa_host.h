@@ -30,6 +30,7 @@ struct FwdArgs {
   int causal;
   float scale;
   int Hkv;  // key/value heads; H % Hkv == 0 (H for plain multi-head attention)
+  int window = 0;  // causal sliding window of this many keys (0: none)
 };
 
 struct BwdArgs {
@@ -46,6 +47,7 @@ struct BwdArgs {
   int causal;
   float scale;
   int Hkv;  // key/value heads of k, v, dk, dv; H % Hkv == 0
+  int window = 0;  // causal sliding window of this many keys (0: none)
 };
 
 fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);

@@ -170,6 +170,21 @@ fa_status fa_fp8_quantize(const void* x, int x_dtype, int hadamard, void* codes,
                           int d, void* stream);
 
 /*
+ * Causal attention with a sliding window ("FLASH-ATTN" lists sliding window
+ * among the variants the kernels support; the pages do not define it, the
+ * reading taken: query i sees keys j with i - window < j <= i, the `window`
+ * most recent keys including its own).  Key blocks entirely outside every
+ * row's window are skipped, so the work grows with N * window, not N^2.
+ *   Arguments, layouts, results and errors as fa_fwd_gqa / fa_bwd_gqa, with
+ *   `window` >= 1 in place of `causal` (window >= N is plain causal attention).
+ */
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                        int N, int d, int window, float scale, void* stream);
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                        void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                        int N, int d, int window, float scale, void* stream);
+
+/*
  * Block sizes of the block-quantised FP8 path: one scale per 128 rows of Q
  * (the forward's query tile, B_r) and per 64 rows of K and of V (its key
  * block, B_c).

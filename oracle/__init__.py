@@ -9,12 +9,14 @@ from .attention import (  # noqa: F401
     LN2,
     backward,
     backward_gqa,
+    backward_window,
     decode,
     flops_backward,
     flops_forward,
     forward,
     forward_fp8_reference,
     forward_gqa,
+    forward_window,
     hadamard_matrix,
     dequantize_e4m3_blocks,
     quantize_e4m3_blocks_reference,

@@ -325,6 +325,68 @@ def dequantize_e4m3_blocks(codes, deltas, block_rows: int):
 
 
 # ---------------------------------------------------------------------------
+# Causal sliding window.
+# ---------------------------------------------------------------------------
+
+def _window_bias(n: int, window: int) -> np.ndarray:
+    """0 where query i sees key j (i - window < j <= i), -inf elsewhere.
+    "FLASH-ATTN" names sliding window among the supported mask variants; the
+    pages give no definition, this is the reading taken (the `window` most
+    recent keys, the query's own included)."""
+    i = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    return np.where((j <= i) & (j > i - window), 0.0, -np.inf)
+
+
+def forward_window(q, k, v, window: int, scale: float):
+    """O [B,H,N,d], L [B,H,N] (float64) of causal sliding-window attention:
+    the definition S = scale Q K^T + mask, P = softmax(S), O = P V,
+    L = m + ln l, with the window mask above; k and v may have fewer heads
+    (grouped queries, head h reads h // (H // Hkv))."""
+    q, k, v = _f64(q), _expand_kv(k, _f64(q).shape[1]), _expand_kv(v, _f64(q).shape[1])
+    B, H, N, _ = q.shape
+    bias = _window_bias(N, window)
+    o = np.empty(q.shape[:3] + (v.shape[-1],))
+    lse = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            s = scale * (q[b, h] @ k[b, h].T) + bias
+            m, f, ell = softmax_stats(s)
+            o[b, h] = (f / ell[:, None]) @ v[b, h]
+            lse[b, h] = m + np.log(ell)
+    return o, lse
+
+
+def backward_window(q, k, v, do, window: int, scale: float):
+    """dQ [B,H,N,d] and dK, dV [B,Hkv,N,d] (float64) of forward_window: the
+    five products of the backward with P from the windowed softmax; dK and dV
+    of a shared key/value head are summed over its query heads."""
+    H = _f64(q).shape[1]
+    Hkv = _f64(k).shape[1]
+    q, do = _f64(q), _f64(do)
+    kx, vx = _expand_kv(k, H), _expand_kv(v, H)
+    B, _, N, _ = q.shape
+    bias = _window_bias(N, window)
+    dq = np.empty_like(q)
+    dkx = np.empty_like(kx)
+    dvx = np.empty_like(vx)
+    for b in range(B):
+        for h in range(H):
+            s = scale * (q[b, h] @ kx[b, h].T) + bias
+            m, f, ell = softmax_stats(s)
+            p = f / ell[:, None]
+            dvx[b, h] = p.T @ do[b, h]
+            dp = do[b, h] @ vx[b, h].T
+            ds = p * (dp - (p * dp).sum(axis=1)[:, None])
+            dq[b, h] = scale * (ds @ kx[b, h])
+            dkx[b, h] = scale * (ds.T @ q[b, h])
+    g = H // Hkv
+    dk = dkx.reshape(B, Hkv, g, N, -1).sum(axis=2)
+    dv = dvx.reshape(B, Hkv, g, N, -1).sum(axis=2)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
 # Decode: one query row against a key/value cache.
 # ---------------------------------------------------------------------------
 

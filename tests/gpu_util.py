@@ -40,3 +40,13 @@ def rel_fro(got, ref):
     g, r = g[sel], r[sel]
     floor = REL_FRO_FLOOR_RMS * np.sqrt(max(r.size, 1))
     return float(np.linalg.norm(g - r) / max(np.linalg.norm(r), floor))
+
+
+def o_rounding_bound(o_ref, v):
+    """Per-element bound on |O - O_ref| that follows from the kernel's
+    arithmetic: P is rounded to bf16 before P V (relative 2^-9 per entry, and
+    l is summed from the unrounded values: 2^-8 max|V| in total) and O is
+    rounded to bf16 on output (half an ulp of |O|)."""
+    import numpy as np
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(o_ref), 1e-30))) - 8)
+    return half_ulp + 2.0 ** -8 * float(f64(v).__abs__().max()) + 1e-4

@@ -9,8 +9,8 @@ import torch
 
 import oracle
 from exact_attention_76_gb300 import api, build, inputs
-from tests.gpu_util import (FP8_O_REL_FRO, GRAD_REL_FRO, L_MAX_ABS, O_MAX_ABS, f64, max_abs, rel_fro,
-                            to_dev)
+from tests.gpu_util import (FP8_O_REL_FRO, GRAD_REL_FRO, L_MAX_ABS, O_MAX_ABS, f64, max_abs, o_rounding_bound,
+                            rel_fro, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -333,6 +333,72 @@ def test_fp8_blocks_forward_with_incoherent_processing(causal):
     o_ref, l_ref = oracle.forward_fp8_reference(q, k, v, causal, scale)
     e = rel_fro(f64(o), o_ref)
     assert e <= FP8_O_REL_FRO, f"block FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
+
+
+# ---------------------------------------------------------------- sliding window
+
+WINDOW_CASES = [
+    # (B, H, Hkv, N, d, window)
+    (1, 2, 2, 256, 64, 63),     # window edge inside a 64-key block
+    (1, 2, 2, 256, 64, 64),
+    (1, 2, 2, 256, 128, 1),     # each row sees only its own key
+    (1, 4, 2, 1000, 128, 100),  # grouped queries, ragged tail
+    (1, 2, 2, 1000, 128, 257),  # window spans tiles; the second tile starts later
+    (2, 2, 1, 777, 64, 700),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,window", WINDOW_CASES)
+def test_window_forward_backward(B, H, Hkv, N, d, window):
+    q, k, v, do = inputs.draw_bf16(B, H, N, d, seed=window)
+    k, v = k[:, :Hkv].contiguous(), v[:, :Hkv].contiguous()
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    o, lse = api.fa_fwd_window(qd, kd, vd, window, scale)
+    dq, dk, dv = api.fa_bwd_window(qd, kd, vd, o, lse, dod, window, scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.forward_window(q, k, v, window, scale)
+    # A row averages at most `window` values, so |O| is larger than under full
+    # attention and its bf16 rounding can pass the 1e-2 of the N(0,1) gate:
+    # the bound is the one that follows from the arithmetic.
+    assert np.all(np.abs(f64(o) - o_ref) <= np.maximum(O_MAX_ABS, o_rounding_bound(o_ref, v)))
+    assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
+    refs = oracle.backward_window(q, k, v, do, window, scale)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), refs):
+        e = rel_fro(f64(g), r)
+        assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e}"
+
+
+def test_window_at_least_n_is_causal_bit_for_bit():
+    q, k, v, do = to_dev(*inputs.draw_bf16(1, 2, 500, 128, seed=21))
+    o1, l1 = api.fa_fwd(q, k, v, True, 0.1)
+    o2, l2 = api.fa_fwd_window(q, k, v, 500, 0.1)
+    dq1, dk1, dv1 = api.fa_bwd(q, k, v, o1, l1, do, True, 0.1)
+    dq2, dk2, dv2 = api.fa_bwd_window(q, k, v, o2, l2, do, 10 ** 6, 0.1)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # dQ sums fp32 contributions in an order that varies run to run
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    assert (dq1.float() - dq2.float()).abs().max().item() <= 2e-3
+
+
+def test_window_long_sequence_sampled_heads():
+    B, H, N, d, window = 1, 4, 4096, 128, 512
+    q, k, v, do = inputs.draw_bf16(B, H, N, d, seed=22)
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    o, lse = api.fa_fwd_window(qd, kd, vd, window, scale)
+    dq, dk, dv = api.fa_bwd_window(qd, kd, vd, o, lse, dod, window, scale)
+    torch.cuda.synchronize()
+    h = 3
+    sl = slice(h, h + 1)
+    o_ref, l_ref = oracle.forward_window(q[:, sl], k[:, sl], v[:, sl], window, scale)
+    assert np.all(np.abs(f64(o[:, sl]) - o_ref) <= np.maximum(O_MAX_ABS, o_rounding_bound(o_ref, v[:, sl])))
+    assert max_abs(f64(lse[:, sl]), l_ref) <= L_MAX_ABS
+    refs = oracle.backward_window(q[:, sl], k[:, sl], v[:, sl], do[:, sl], window, scale)
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq[:, sl], dk[:, sl], dv[:, sl]), refs):
+        e = rel_fro(f64(g), r)
+        assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e}"
 
 
 # ---------------------------------------------------------------- decode

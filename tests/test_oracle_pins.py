@@ -396,6 +396,61 @@ def test_e4m3_blocks_rounding_bound_and_zero_block():
     np.testing.assert_allclose(deltas, np.where(amax > 0, amax / 448.0, 1.0), rtol=1e-15)
 
 
+# ---------------------------------------------------------------- sliding window
+
+def test_window_covering_the_sequence_is_causal_attention():
+    q, k, v, do = (t.double().numpy() for t in inputs.draw_fp32(1, 2, 30, 8, 13))
+    o_c, l_c = oracle.forward(q, k, v, True, 0.3)
+    for w in (30, 31, 100):
+        o_w, l_w = oracle.forward_window(q, k, v, w, 0.3)
+        np.testing.assert_array_equal(o_w, o_c)
+        np.testing.assert_array_equal(l_w, l_c)
+    dq, dk, dv = oracle.backward(q, k, v, do, True, 0.3)
+    dq2, dk2, dv2 = oracle.backward_window(q, k, v, do, 30, 0.3)
+    for a, b in ((dq, dq2), (dk, dk2), (dv, dv2)):
+        np.testing.assert_allclose(b, a, rtol=0, atol=1e-13)
+
+
+def test_window_of_one_and_two_closed_forms():
+    q, k, v, do = (t.double().numpy() for t in inputs.draw_fp32(1, 1, 12, 4, 14))
+    s = 0.7
+    # window 1: every query sees only its own key
+    o, lse = oracle.forward_window(q, k, v, 1, s)
+    np.testing.assert_allclose(o, v, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[0, 0], s * np.einsum("nd,nd->n", q[0, 0], k[0, 0]), rtol=0, atol=1e-13)
+    dq, dk, dv = oracle.backward_window(q, k, v, do, 1, s)
+    np.testing.assert_allclose(dv, do, rtol=0, atol=1e-15)
+    assert np.abs(dq).max() < 1e-14 and np.abs(dk).max() < 1e-14
+    # window 2: a two-way softmax over keys i-1 and i
+    o, _ = oracle.forward_window(q, k, v, 2, s)
+    qq, kk, vv = q[0, 0], k[0, 0], v[0, 0]
+    for i in range(1, 12):
+        a, b = s * qq[i] @ kk[i - 1], s * qq[i] @ kk[i]
+        w = 1.0 / (1.0 + math.exp(b - a))  # weight of key i-1
+        np.testing.assert_allclose(o[0, 0, i], w * vv[i - 1] + (1 - w) * vv[i], rtol=0, atol=1e-13)
+
+
+def test_window_backward_finite_differences():
+    q, k, v, do = (t.double().numpy() for t in inputs.draw_fp32(1, 2, 10, 4, 15))
+    k, v = k[:, :1], v[:, :1]  # two query heads share one key/value head
+    w, s, h = 3, 0.5, 1e-6
+    dq, dk, dv = oracle.backward_window(q, k, v, do, w, s)
+
+    def loss(q_, k_, v_):
+        return float((oracle.forward_window(q_, k_, v_, w, s)[0] * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in [(0, 0, 3, 1), (0, 0, 9, 2), (0, x.shape[1] - 1, 5, 0)]:
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            fd = (loss(**{a + "_": b for a, b in args_p.items()}) - loss(**{a + "_": b for a, b in args_m.items()})) / (2 * h)
+            assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(g[idx])), (name, idx, fd, g[idx])
+
+
 # ---------------------------------------------------------------- decode
 
 def test_decode_is_the_last_row_of_causal_attention():
