@@ -386,6 +386,47 @@ def run_ours(args):
     return 0
 
 
+def run_decode(args):
+    """Decode against a key/value cache (a side measurement, not the bench's
+    workload): K/V read bandwidth of fa_decode, timed with CUDA events on the
+    launching stream; the cache (2 B H_kv N d bf16) is meant to exceed L2."""
+    import torch
+
+    from exact_attention_76_gb300 import api
+    from exact_attention_76_gb300 import build as _build
+
+    _build.build()
+    B, H, Hkv, N, d = (int(x) for x in args.decode.split(","))
+    g = torch.Generator(device="cuda").manual_seed(1)
+    q = torch.randn(B, H, d, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, N, d, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, N, d, device="cuda", generator=g).to(torch.bfloat16)
+    ws = torch.empty(api.fa_decode_workspace_size(B, H, Hkv, N, d), dtype=torch.uint8, device="cuda")
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, H, dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        api.fa_decode(q, k, v, scale, o=o, lse=lse, workspace=ws, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        api.fa_decode(q, k, v, scale, o=o, lse=lse, workspace=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    kv_bytes = 2.0 * B * Hkv * N * d * 2
+    gbs = kv_bytes / ms / 1e6
+    peaks, src = measured_peaks()
+    print(json.dumps({"metric": "decode K/V read bandwidth", "value": gbs, "unit": "GB/s", "steps": args.steps,
+                      "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": f"decode_B{B}_H{H}_Hkv{Hkv}_N{N}_d{d}", "kv_bytes": kv_bytes},
+                      "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": gbs / peaks["hbm_gbs"], "peak_source": src}}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,7 +436,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--shape", default="", help="B,H,N,d of a causal profiling case instead of the workload")
+    ap.add_argument("--decode", default="", help="B,H,Hkv,N,d: time fa_decode instead (side measurement)")
     args = ap.parse_args()
+    if args.decode:
+        return run_decode(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
