@@ -18,6 +18,7 @@ from .attention import (  # noqa: F401
     forward_gqa,
     forward_window,
     hadamard_matrix,
+    dequantize_e4m3,
     dequantize_e4m3_blocks,
     quantize_e4m3_blocks_reference,
     quantize_e4m3_reference,

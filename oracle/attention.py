@@ -287,6 +287,13 @@ def quantize_e4m3_reference(x):
     return y.to(torch.float8_e4m3fn).view(torch.uint8).numpy(), delta
 
 
+def dequantize_e4m3(codes, delta: float):
+    """x ~= delta * e4m3(code), float64: the inverse of the per-tensor storage."""
+    import torch
+    c = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return c * float(delta)
+
+
 def quantize_e4m3_blocks_reference(x, block_rows: int):
     """Block e4m3 storage ("FLASH-ATTN", FlashAttention-3 > Low-precision with
     FP8, block quantisation: Q, K and V are cut into blocks of B_r x d or

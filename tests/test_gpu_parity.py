@@ -180,12 +180,12 @@ def test_backward_in_three_calls_matches_fa_bwd():
 def _fp8_case(N, causal, seed=4, B=1, H=2, d=128):
     q, k, v = inputs.draw_outlier_fp32(B, H, N, d, seed=seed)
     codes, deltas = [], []
-    for t in (q, k, v):
-        c, dl = inputs.quantize_e4m3_per_tensor(t)
+    for t in (q, k, v):  # per-tensor e4m3 storage, made by the oracle's quantiser
+        c, dl = oracle.quantize_e4m3_reference(t)
         codes.append(c)
-        deltas.append(dl)
+        deltas.append(float(np.float32(dl)))
     scale = 1 / math.sqrt(d)
-    q8, k8, v8 = to_dev(*codes)
+    q8, k8, v8 = (torch.from_numpy(c).cuda() for c in codes)
     dsc = [torch.tensor([x], dtype=torch.float32, device="cuda") for x in deltas]
     o, lse = api.fa_fwd_fp8(q8, k8, v8, *dsc, causal, scale)
     torch.cuda.synchronize()
@@ -198,7 +198,7 @@ def test_fp8_forward_kernel_error(causal, N):
     # Against exact attention on the dequantised e4m3 inputs: what remains is
     # the kernel's own error (P stored as e4m3, fp32 accumulation).
     orig, codes, deltas, o, lse, scale = _fp8_case(N, causal)
-    deq = [inputs.e4m3_codes_to_fp32(c) * dl for c, dl in zip(codes, deltas)]
+    deq = [oracle.dequantize_e4m3(c, dl) for c, dl in zip(codes, deltas)]
     o_deq, l_deq = oracle.forward(*deq, causal, scale)
     e = rel_fro(f64(o), o_deq)
     assert e <= FP8_O_REL_FRO, f"FP8 O rel-Frobenius vs dequantised inputs {e:.3e}"
@@ -399,6 +399,48 @@ def test_window_long_sequence_sampled_heads():
     for name, g, r in zip(("dQ", "dK", "dV"), (dq[:, sl], dk[:, sl], dv[:, sl]), refs):
         e = rel_fro(f64(g), r)
         assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e}"
+
+
+# ---------------------------------------------------------------- random configurations
+
+def _random_config(seed):
+    r = np.random.default_rng(1000 + seed)
+    d = int(r.choice([64, 128]))
+    Hkv = int(r.choice([1, 2, 3]))
+    H = Hkv * int(r.choice([1, 2, 4]))
+    N = int(r.choice([1, 2, 3, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 511, 640, 700]))
+    mode = str(r.choice(["full", "causal", "window"]))
+    window = int(r.integers(1, 2 * N + 2)) if mode == "window" else 0
+    return int(r.integers(1, 3)), H, Hkv, N, d, mode, window
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_configurations(seed):
+    # Seeded random shapes (ragged lengths down to one token, grouped heads,
+    # both head sizes, full / causal / windowed) through the public entry
+    # points, forward and backward, against the oracle.
+    B, H, Hkv, N, d, mode, window = _random_config(seed)
+    q, k, v, do = inputs.draw_bf16(B, H, N, d, seed=seed)
+    k, v = k[:, :Hkv].contiguous(), v[:, :Hkv].contiguous()
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    if mode == "window":
+        o, lse = api.fa_fwd_window(qd, kd, vd, window, scale)
+        dq, dk, dv = api.fa_bwd_window(qd, kd, vd, o, lse, dod, window, scale)
+        o_ref, l_ref = oracle.forward_window(q, k, v, window, scale)
+        refs = oracle.backward_window(q, k, v, do, window, scale)
+    else:
+        causal = mode == "causal"
+        o, lse = api.fa_fwd_gqa(qd, kd, vd, causal, scale)
+        dq, dk, dv = api.fa_bwd_gqa(qd, kd, vd, o, lse, dod, causal, scale)
+        o_ref, l_ref = oracle.forward_gqa(q, k, v, causal, scale)
+        refs = oracle.backward_gqa(q, k, v, do, causal, scale)
+    torch.cuda.synchronize()
+    assert np.all(np.abs(f64(o) - o_ref) <= np.maximum(O_MAX_ABS, o_rounding_bound(o_ref, v)))
+    assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), refs):
+        e = rel_fro(f64(g), r)
+        assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e} ({B},{H},{Hkv},{N},{d},{mode},{window})"
 
 
 # ---------------------------------------------------------------- decode

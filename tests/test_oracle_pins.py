@@ -299,18 +299,6 @@ def test_inputs_are_deterministic_and_bf16():
     assert not torch.equal(a[0], c[0])
 
 
-def test_fp8_quantisation_roundtrip():
-    x = inputs.draw_outlier_fp32(1, 2, 512, 64, 4)[0]
-    codes, delta = inputs.quantize_e4m3_per_tensor(x)
-    assert codes.dtype == torch.uint8
-    deq = inputs.e4m3_codes_to_fp32(codes) * delta
-    assert abs(float(deq.abs().max()) - float(x.abs().max())) <= 1e-6 * float(x.abs().max())
-    # e4m3 has 3 mantissa bits: relative rounding error <= 2^-4 on normals
-    big = x.abs() > 2 ** -6 * delta * 4
-    rel = ((deq - x).abs() / x.abs())[big]
-    assert float(rel.max()) <= 2 ** -4 + 1e-6
-
-
 # ---------------------------------------------------------------- FP8 storage
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -342,6 +330,7 @@ def test_e4m3_reference_quantiser():
     codes, delta = oracle.quantize_e4m3_reference(x)
     assert abs(delta - np.abs(x).max() / 448.0) < 1e-15
     deq = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy() * delta
+    np.testing.assert_array_equal(oracle.dequantize_e4m3(codes, delta), deq)
     # the amax entry maps to 448 exactly; normals are within half an e4m3 ulp (2^-4 relative)
     assert abs(np.abs(deq).max() - np.abs(x).max()) <= 1e-12 * np.abs(x).max()
     big = np.abs(x) >= 2.0 ** -6 * delta
