@@ -61,6 +61,8 @@ struct DecSmem {
   uint64_t empty[kDecSlots];
   float m[16];
   float l[16];
+  float red_m[8][16];  // per compute warp and head
+  float red_l[8][16];
   CtaAbort abort;
 };
 
@@ -167,6 +169,11 @@ __global__ void __launch_bounds__(kDecThreads, 3)
   };
 
   // Pass 1: scores.  Thread t: key k = t / 4 of the tile, quarter p = t % 4.
+  // Each thread also keeps the running maximum of the heads it stores
+  // (h % 4 == p).
+  float mloc[G4 / 4];
+#pragma unroll
+  for (int i = 0; i < G4 / 4; ++i) mloc[i] = -INFINITY;
   {
     const int k = t >> 2, p = t & 3;
     const float* qp = s_q + p * Cf::kQStride;
@@ -203,34 +210,73 @@ __global__ void __launch_bounds__(kDecThreads, 3)
           float v = acc[h].x + acc[h].y;
           v += __shfl_xor_sync(0xffffffffu, v, 1);
           v += __shfl_xor_sync(0xffffffffu, v, 2);
-          if ((h & 3) == p) s_score[key * gp + h] = valid ? v : -INFINITY;
+          if ((h & 3) == p) {
+            s_score[key * gp + h] = valid ? v : -INFINITY;
+            if (valid) mloc[h >> 2] = fmaxf(mloc[h >> 2], v);
+          }
         }
       }
     }
   }
-  named_bar_sync(1, kDecCompute);
-
-  // Per head: m = max over the chunk, p = 2^(s - m) in place, l = sum p.
-  const int n_keys = n_tiles * kDecTile;
-  for (int h = warp; h < g; h += kDecCompute / 32) {
-    float m = -INFINITY;
-    for (int key = lane_id(); key < n_keys; key += 32) m = fmaxf(m, s_score[key * gp + h]);
+  // Per head: m = max over the chunk (from the threads' running maxima),
+  // p = 2^(s - m) in place over all threads, l = sum p.
+  {
+    const int p = t & 3;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float l = 0.f;
-    for (int key = lane_id(); key < n_keys; key += 32) {
-      const float pv = ex2_approx(s_score[key * gp + h] - m);
-      s_score[key * gp + h] = pv;
-      l += pv;
-    }
+    for (int i = 0; i < G4 / 4; ++i) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    if (lane_id() == 0) {
-      sh.m[h] = m;
-      sh.l[h] = l;
+      for (int off = 4; off < 32; off <<= 1)  // lanes of the same p
+        mloc[i] = fmaxf(mloc[i], __shfl_xor_sync(0xffffffffu, mloc[i], off));
+      if (lane_id() < 4) sh.red_m[warp][4 * i + p] = mloc[i];
     }
   }
   named_bar_sync(1, kDecCompute);
+  float m[G4], l[G4];
+#pragma unroll
+  for (int h = 0; h < G4; ++h) {
+    float mm = sh.red_m[0][h];
+#pragma unroll
+    for (int w = 1; w < kDecCompute / 32; ++w) mm = fmaxf(mm, sh.red_m[w][h]);
+    m[h] = mm == -INFINITY ? 0.0f : mm;  // padded heads: no keys
+    l[h] = 0.f;
+  }
+  const int n_keys = n_tiles * kDecTile;
+  for (int key = t; key < n_keys; key += kDecCompute) {
+#pragma unroll
+    for (int h4 = 0; h4 < G4; h4 += 4) {
+      if (h4 < gp) {
+        float4 s4 = *reinterpret_cast<const float4*>(s_score + key * gp + h4);
+        s4.x = ex2_approx(s4.x - m[h4]);
+        s4.y = ex2_approx(s4.y - m[h4 + 1]);
+        s4.z = ex2_approx(s4.z - m[h4 + 2]);
+        s4.w = ex2_approx(s4.w - m[h4 + 3]);
+        *reinterpret_cast<float4*>(s_score + key * gp + h4) = s4;
+        l[h4] += s4.x;
+        l[h4 + 1] += s4.y;
+        l[h4 + 2] += s4.z;
+        l[h4 + 3] += s4.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G4; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+    if (lane_id() == 0) sh.red_l[warp][h] = l[h];
+  }
+  named_bar_sync(1, kDecCompute);
+  if (t == 0) {  // unrolled over heads: m stays in registers
+#pragma unroll
+    for (int h = 0; h < G4; ++h) {
+      if (h < g) {
+        float ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecCompute / 32; ++w) ls += sh.red_l[w][h];
+        sh.m[h] = m[h];
+        sh.l[h] = ls;
+      }
+    }
+  }
 
   // Pass 2: O_h += sum_k p_hk v_k.  Thread t: column pair cp, key group kg.
   const int cp = t % Cf::kPairs, kg = t / Cf::kPairs;
