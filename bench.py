@@ -49,25 +49,34 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_source_hash():
+# Source files each timed kernel is compiled from (its translation unit and
+# the headers it includes).
+KERNEL_SOURCES = {
+    "fa_fwd": ["fa_fwd.cu", "fa_common.cuh", "fa_host.h"],
+    "fa_bwd_preprocess": ["fa_bwd.cu", "fa_common.cuh", "fa_host.h"],
+    "fa_bwd_main": ["fa_bwd.cu", "fa_common.cuh", "fa_host.h"],
+    "fa_bwd_dq_convert": ["fa_bwd.cu", "fa_common.cuh", "fa_host.h"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_76_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since those counters were taken."""
+    kernel's sources changed since those counters were taken."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as f:
         rec = json.load(f)
     ent = rec.get("kernels", {}).get(kernel)
-    if not ent or rec.get("source_hash") != kernel_source_hash():
+    if not ent or kernel not in KERNEL_SOURCES or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
