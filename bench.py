@@ -446,9 +446,18 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--shape", default="", help="B,H,N,d of a causal profiling case instead of the workload")
     ap.add_argument("--decode", default="", help="B,H,Hkv,N,d: time fa_decode instead (side measurement)")
+    ap.add_argument("--mufu", action="store_true", help="measure the special-function unit's exp2 rate")
     args = ap.parse_args()
     if args.decode:
         return run_decode(args)
+    if args.mufu:
+        from exact_attention_76_gb300 import api
+        from exact_attention_76_gb300 import build as _build
+        _build.build()
+        rate = api.fa_measure_ex2_rate()
+        print(json.dumps({"metric": "ex2 rate", "value": rate, "unit": "results/clock/SM",
+                          "note": "2 CTAs x 512 threads per SM, 8 independent ex2->FMA chains per thread"}))
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -39,6 +39,7 @@ SIGNATURES = {
     "fa_fp8_quantize_blocks": ([_P, _I, _I, _I, _P, _P, _I, _I, _I, _P], _I),
     "fa_fwd_window": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "fa_bwd_window": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _I, _F, _P], _I),
+    "fa_measure_ex2_rate": ([_P, _P], _I),
     "fa_decode_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "fa_decode": ([_P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _F, _P], _I),
 }

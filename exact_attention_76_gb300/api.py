@@ -313,6 +313,14 @@ def fa_decode(q, k, v, scale: float, o=None, lse=None, workspace=None, stream=No
     return o, lse
 
 
+def fa_measure_ex2_rate(stream=None) -> float:
+    """exp2 results per clock per SM of the special-function unit (a measurement)."""
+    import ctypes
+    out = ctypes.c_float(0.0)
+    _lib.check("fa_measure_ex2_rate", _lib.load().fa_measure_ex2_rate(ctypes.byref(out), _stream_ptr(stream)))
+    return float(out.value)
+
+
 def fa_status_string(status: int) -> str:
     return _lib.load().fa_status_string(int(status)).decode()
 

@@ -106,6 +106,34 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, int col
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Special-function-unit rate: every thread runs 8 independent chains
+// x <- 0.5 - 2^x (each step one ex2 and one FMA; x stays in [-1, 0.5]).  One
+// CTA's cycle count is taken between two CTA barriers, so the rate is per SM
+// with every CTA of the SM running.
+__global__ void __launch_bounds__(512) ex2_rate_kernel(int iters, float* sink, long long* cycles) {
+  float x[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) x[c] = -0.125f * static_cast<float>((threadIdx.x + c) & 7);
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) x[c] = fmaf(-1.0f, ex2_approx(x[c]), 0.5f);
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float acc = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc += x[c];
+  sink[blockIdx.x * blockDim.x + threadIdx.x] = acc;
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+fa_status launch_ex2_rate(int blocks, int iters, float* sink, long long* cycles, cudaStream_t stream) {
+  ex2_rate_kernel<<<blocks, 512, 0, stream>>>(iters, sink, cycles);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 fa_status launch_timeout_probe(unsigned int limit_us, cudaStream_t stream) {
   int dev = 0, khz = 2000000;
   cudaGetDevice(&dev);
@@ -352,6 +380,43 @@ fa_status fa_device_error(void* stream) {
   if (e & FA_DEVERR_TIMEOUT) return FA_ERR_TIMEOUT;
   if (e != 0) return FA_ERR_LAUNCH;
   return FA_OK;
+}
+
+fa_status fa_measure_ex2_rate(float* ex2_per_clock_per_sm, void* stream) {
+  fa_status st;
+  if (ex2_per_clock_per_sm == nullptr) return FA_ERR_INVALID_ARG;
+  if ((st = check_device()) != FA_OK) return st;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int blocks = 2 * sms, iters = 4096;  // two CTAs of 512 threads per SM
+  float* sink = nullptr;
+  long long* cycles = nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMallocAsync(reinterpret_cast<void**>(&sink), sizeof(float) * blocks * 512, s) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&cycles), sizeof(long long) * blocks, s) != cudaSuccess) {
+    cudaFreeAsync(sink, s);
+    return FA_ERR_LAUNCH;
+  }
+  st = launch_ex2_rate(blocks, iters, sink, cycles, s);  // warm-up
+  if (st == FA_OK) st = launch_ex2_rate(blocks, iters, sink, cycles, s);
+  long long* host = new long long[blocks];
+  if (st == FA_OK && (cudaMemcpyAsync(host, cycles, sizeof(long long) * blocks, cudaMemcpyDeviceToHost, s) !=
+                          cudaSuccess ||
+                      cudaStreamSynchronize(s) != cudaSuccess))
+    st = FA_ERR_LAUNCH;
+  if (st == FA_OK) {
+    long long worst = 1;
+    for (int b = 0; b < blocks; ++b) worst = host[b] > worst ? host[b] : worst;
+    // two CTAs per SM shared the SM for `worst` cycles
+    *ex2_per_clock_per_sm = static_cast<float>(2.0 * 512.0 * 8.0 * iters / static_cast<double>(worst));
+  }
+  delete[] host;
+  cudaFreeAsync(sink, s);
+  cudaFreeAsync(cycles, s);
+  cudaStreamSynchronize(s);
+  return st;
 }
 
 fa_status fa_debug_wait_timeout(unsigned int limit_us, void* stream) {

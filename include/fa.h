@@ -285,6 +285,16 @@ const char* fa_status_string(fa_status s);
 fa_status fa_device_error(void* stream);
 
 /*
+ * Measurement hook: the special-function unit's exp2 rate on this GPU, in
+ * results per clock per SM (two CTAs of 512 threads per SM, each thread 8
+ * independent ex2 -> FMA chains).  The softmax of every kernel here costs one
+ * exp2 per score, so this rate bounds it ("FLASH-ATTN", FlashAttention-3:
+ * the exponential unit is far slower than the tensor cores).  Allocates and
+ * frees its scratch on `stream` and synchronises it.
+ */
+fa_status fa_measure_ex2_rate(float* ex2_per_clock_per_sm, void* stream);
+
+/*
  * Test hook for the timeout path: launches one CTA whose thread waits on an
  * mbarrier that nothing ever completes, with a limit of about `limit_us`
  * microseconds (1..1000000); the kernel records a timeout and returns.  A

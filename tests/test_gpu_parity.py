@@ -521,6 +521,13 @@ def test_timeout_path_reports_and_context_survives():
     check_fwd(o, lse, q, k, v, False, 0.125)
 
 
+def test_ex2_rate_measurement():
+    # a rate per SM and clock: positive and below one result per lane of the
+    # SM's four 32-lane sub-partitions
+    rate = api.fa_measure_ex2_rate()
+    assert 1.0 < rate <= 128.0
+
+
 def test_python_argument_checks():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.float16, device="cuda")
     with pytest.raises(TypeError):
