@@ -381,14 +381,317 @@ fa_status launch_decode_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStre
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+
+// ---------------------------------------------------------------------------
+// Grouped heads (4..16 query heads per key/value head, d = 128): the score and
+// P.V products are real contractions over the group, (keys x d)(d x heads)
+// and (d x keys)(keys x heads), so they go to the tensor cores, which leaves
+// the kernel bound by the cache read again.
+//   warps 0-3 : one key of a 128-key tile per thread (TMEM lane); pass 1
+//               reads S^T and keeps per-head maxima, pass 2 forms P and
+//               writes it to shared memory as the B operand of P.V; at the
+//               end thread t reads column d = t of O^T.
+//   warp 4    : TMA producer (K tiles, then V tiles, 3-slot ring).
+//   warp 5    : TMEM allocation and the MMA-issuing thread.
+// S^T = K Q^T (M = 128 keys, N = 16 padded heads, A = K tile K-major, B = Q
+// K-major) in TMEM columns 16 t; O^T += V^T P^T (M = d, N = 16, A = V tile
+// read MN-major, B = P K-major) in columns 128.. .
+constexpr int kTcThreads = 192;
+constexpr int kTcTile = 128;           // keys per tile
+constexpr int kTcSlots = 3;
+constexpr int kTcTileBytes = kTcTile * 128 * 2;  // 32 KB (d = 128)
+constexpr int kTcBlockBytes = kTcTile * 128;     // one 64-column block of a tile
+constexpr int kTcMaxTiles = 8;         // chunk <= 1024 keys
+constexpr int kTcN = 16;               // padded heads
+constexpr int kTcPBytes = kTcN * kTcTile * 2;    // 4 KB: P of one tile (16 x 128 bf16)
+constexpr int kTcQBytes = kTcN * 128 * 2;        // 4 KB
+constexpr uint32_t kTcTmO = 128;
+constexpr int kTcSmem = 1024 + kTcSlots * kTcTileBytes + 2 * kTcPBytes + kTcQBytes;
+
+struct DecTcSmem {
+  uint64_t full[kTcSlots];
+  uint64_t empty[kTcSlots];
+  uint64_t s_full[kTcMaxTiles];
+  uint64_t p_full[2];
+  uint64_t p_empty[2];
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  float red[4][kTcN];
+  float m[kTcN];
+  float l[kTcN];
+  CtaAbort abort;
+};
+
+// Byte offset of (row r, element e) in a K-major tile of `rows` rows stored as
+// 64-element (128-byte) column blocks with the 128-byte swizzle.
+__device__ __forceinline__ int kmaj_off(int r, int e, int rows) {
+  return (e >> 6) * rows * 128 + r * 128 + ((((e & 63) >> 3) ^ (r & 7)) << 4) + ((e & 7) << 1);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fa_decode_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                        const __nv_bfloat16* __restrict__ q, float* __restrict__ part, int H, int Hkv, int N, int C,
+                        int nsplit, float scale_log2) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ DecTcSmem sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_ring = smem;
+  uint8_t* s_p = smem + kTcSlots * kTcTileBytes;  // two P buffers
+  uint8_t* s_qp = s_p + 2 * kTcPBytes;             // padded Q
+
+  if (*reinterpret_cast<volatile uint32_t*>(&g_err_dec) & FA_DEVERR_TIMEOUT) return;
+  const int g = H / Hkv;
+  const int chunk = static_cast<int>(blockIdx.x);
+  const int bkv = static_cast<int>(blockIdx.y);
+  const int key_begin = chunk * C;
+  const int key_end = min(N, key_begin + C);
+  const int n_tiles = (key_end - key_begin + kTcTile - 1) / kTcTile;
+  const int bq0 = (bkv / Hkv) * H + (bkv % Hkv) * g;
+  const int warp = static_cast<int>(warp_id());
+  const int t = threadIdx.x;
+
+  if (t == 0) {
+    sh.abort.flag = 0;
+    for (int i = 0; i < kTcSlots; ++i) {
+      mbar_init(&sh.full[i], 1);
+      mbar_init(&sh.empty[i], 1);
+    }
+    for (int i = 0; i < kTcMaxTiles; ++i) mbar_init(&sh.s_full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.p_full[i], 128);
+      mbar_init(&sh.p_empty[i], 1);
+    }
+    mbar_init(&sh.o_done, 1);
+    mbar_init(&sh.drain, 1);
+    fence_barrier_init();
+  }
+  // Q of the group as a 16-row K-major bf16 tile (rows past g are zero).
+  for (int i = t; i < kTcN * 128; i += kTcThreads) {
+    const int h = i >> 7, e = i & 127;
+    const __nv_bfloat16 val = h < g ? q[static_cast<size_t>(bq0 + h) * 128 + e] : __float2bfloat16_rn(0.f);
+    *reinterpret_cast<__nv_bfloat16*>(s_qp + kmaj_off(h, e, kTcN)) = val;
+  }
+  fence_proxy_async_smem();  // generic-proxy stores -> tensor core reads
+  if (warp == 5) tmem_alloc(&sh.tmem_base, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      int issued = 0;
+      for (int it = 0; it < 2 * n_tiles && !sh.abort.flag; ++it) {
+        const int slot = issued % kTcSlots;
+        const int round = issued / kTcSlots;
+        if (round > 0 && !mbar_wait<true>(&sh.empty[slot], (round - 1) & 1, &sh.abort, &g_err_dec)) break;
+        const bool is_k = it < n_tiles;
+        const int key0 = key_begin + (is_k ? it : it - n_tiles) * kTcTile;
+        mbar_arrive_expect_tx(&sh.full[slot], kTcTileBytes);
+        for (int cb = 0; cb < 2; ++cb)
+          tma_load_3d(s_ring + slot * kTcTileBytes + cb * kTcBlockBytes, is_k ? &map_k : &map_v, cb * 64, key0, bkv,
+                      &sh.full[slot]);
+        ++issued;
+      }
+      if (sh.abort.flag) {
+        for (int i = 0; i < kTcSlots && i < issued; ++i) {
+          const int last = i + ((issued - 1 - i) / kTcSlots) * kTcSlots;
+          mbar_wait_drain(&sh.full[i], (last / kTcSlots) & 1, &g_err_dec);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t kIdS = idesc_bf16(128, kTcN, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(128, kTcN, true, false);
+      const uint64_t ring_k = sdesc_sw128(smem_u32(s_ring), 16, 1024);             // K tiles, K-major
+      const uint64_t ring_mn = sdesc_sw128(smem_u32(s_ring), kTcBlockBytes, 1024);  // V tiles, MN-major
+      const uint64_t q_k = sdesc_sw128(smem_u32(s_qp), 16, 1024);
+      const uint64_t p_k = sdesc_sw128(smem_u32(s_p), 16, 1024);
+      bool ok = true;
+      int used = 0;
+      for (int tile = 0; ok && tile < n_tiles; ++tile, ++used) {
+        const int slot = used % kTcSlots;
+        ok = mbar_wait<true>(&sh.full[slot], (used / kTcSlots) & 1, &sh.abort, &g_err_dec);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t a0 = sdesc_advance(ring_k, slot * kTcTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_bf16_ss(tmem + tile * kTcN, sdesc_advance(a0, (kk >> 2) * kTcBlockBytes + (kk & 3) * 32),
+                      sdesc_advance(q_k, (kk >> 2) * (kTcN * 128) + (kk & 3) * 32), kIdS, kk > 0);
+        }
+        tc_commit(&sh.s_full[tile]);
+        tc_commit(&sh.empty[slot]);
+      }
+      for (int tile = 0; ok && tile < n_tiles; ++tile, ++used) {
+        const int slot = used % kTcSlots;
+        const int b = tile & 1;
+        ok = mbar_wait<true>(&sh.full[slot], (used / kTcSlots) & 1, &sh.abort, &g_err_dec) &&
+             mbar_wait<true>(&sh.p_full[b], (tile >> 1) & 1, &sh.abort, &g_err_dec);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t a0 = sdesc_advance(ring_mn, slot * kTcTileBytes);
+        const uint64_t b0 = sdesc_advance(p_k, b * kTcPBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_bf16_ss(tmem + kTcTmO, sdesc_advance(a0, kk * 2048),
+                      sdesc_advance(b0, (kk >> 2) * (kTcN * 128) + (kk & 3) * 32), kIdPV, (tile > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&sh.p_empty[b]);
+        tc_commit(&sh.empty[slot]);
+      }
+      if (ok) tc_commit(&sh.o_done);
+      tc_commit(&sh.drain);
+      mbar_wait_drain(&sh.drain, 0, &g_err_dec);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ keys (lanes)
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+    float m[kTcN];
+#pragma unroll
+    for (int h = 0; h < kTcN; ++h) m[h] = -INFINITY;
+    // pass 1: per-head maxima of x = s * scale * log2 e
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      ok = ok && mbar_wait<true>(&sh.s_full[tile], 0, &sh.abort, &g_err_dec);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_base + tile * kTcN, r);
+      tmem_ld_wait(r);
+      if (key_begin + tile * kTcTile + t < key_end) {
+#pragma unroll
+        for (int h = 0; h < kTcN; ++h) m[h] = fmaxf(m[h], __uint_as_float(r[h]) * scale_log2);
+      }
+    }
+    // maxima over the 128 keys of the threads: warp, then the four warps
+#pragma unroll
+    for (int h = 0; h < kTcN; ++h) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], off));
+    }
+    if (lane_id() == 0) {
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) sh.red[warp][h] = m[h];
+    }
+    named_bar_sync(1, 128);
+#pragma unroll
+    for (int h = 0; h < kTcN; ++h) {
+      const float mm = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
+      m[h] = mm == -INFINITY ? 0.0f : mm;  // padded heads (and no visible key) use 0
+    }
+    named_bar_sync(1, 128);  // every thread has read sh.red before it is reused for l
+    // pass 2: P = 2^(x - m) into the B operand of P.V, and l = sum P
+    float l[kTcN];
+#pragma unroll
+    for (int h = 0; h < kTcN; ++h) l[h] = 0.f;
+    for (int tile = 0; ok && tile < n_tiles; ++tile) {
+      const int b = tile & 1;
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_base + tile * kTcN, r);
+      tmem_ld_wait(r);
+      const bool valid = key_begin + tile * kTcTile + t < key_end;
+      if (tile >= 2) {  // the P.V two tiles back has read this buffer
+        ok = mbar_wait<true>(&sh.p_empty[b], ((tile >> 1) - 1) & 1, &sh.abort, &g_err_dec);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      uint8_t* pb = s_p + b * kTcPBytes;
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) {
+        const float pv = valid ? ex2_approx(__uint_as_float(r[h]) * scale_log2 - m[h]) : 0.f;
+        l[h] += pv;
+        *reinterpret_cast<__nv_bfloat16*>(pb + kmaj_off(h, t, kTcN)) = __float2bfloat16_rn(pv);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sh.p_full[b]);
+    }
+#pragma unroll
+    for (int h = 0; h < kTcN; ++h) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+    }
+    if (lane_id() == 0) {
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) sh.red[warp][h] = l[h];
+    }
+    const bool all_ok = named_bar_and(1, 128, ok);
+    if (t == 0) {
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) {
+        sh.m[h] = m[h];
+        sh.l[h] = (sh.red[0][h] + sh.red[1][h]) + (sh.red[2][h] + sh.red[3][h]);
+      }
+    }
+    named_bar_sync(1, 128);
+    if (all_ok && mbar_wait<true>(&sh.o_done, 0, &sh.abort, &g_err_dec)) {
+      tc_fence_after();
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_base + kTcTmO, r);  // thread t: column d = t of O^T
+      tmem_ld_wait(r);
+      const size_t stride = 128 + 4;
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) {
+        if (h < g) {
+          float* row = part + (static_cast<size_t>(bq0 + h) * nsplit + chunk) * stride;
+          row[t] = __uint_as_float(r[h]);
+          if (t == 0) {
+            row[128] = sh.m[h];
+            row[129] = sh.l[h];
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+fa_status launch_decode_tc(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
+  CUtensorMap mk, mv;
+  const int BHkv = a.B * a.Hkv;
+  if (!encode_rows_map(&mk, a.k, 2, 128, a.N, BHkv, 64, kTcTile) ||
+      !encode_rows_map(&mv, a.v, 2, 128, a.N, BHkv, 64, kTcTile))
+    return FA_ERR_LAUNCH;
+  if (cudaFuncSetAttribute(fa_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  const dim3 grid(static_cast<unsigned>(pl.nsplit), static_cast<unsigned>(BHkv));
+  fa_decode_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.q), a.part,
+                                                         a.H, a.Hkv, a.N, pl.chunk, pl.nsplit,
+                                                         a.scale * 1.4426950408889634f);
+  const int rows = a.B * a.H;
+  fa_decode_merge_kernel<128><<<(rows + 7) / 8, 256, 0, s>>>(a.part, static_cast<__nv_bfloat16*>(a.o), a.lse, rows,
+                                                            pl.nsplit);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+bool use_tc(int g, int d) { return d == 128 && g >= 4; }
+
 }  // namespace
 
 DecodePlan decode_plan(int B, int H, int Hkv, int N, int d) {
-  (void)d;
   const int g = H / Hkv;
   const int gp = (g + 3) & ~3;
-  // chunk keys: the score buffer holds chunk x gp floats; at most 1024 keys
-  int cmax = (kDecScoreBytes / 4 / gp) / kDecTile * kDecTile;
+  const bool tc = use_tc(g, d);
+  const int tile = tc ? kTcTile : kDecTile;
+  // chunk keys: the score buffer holds chunk x gp floats (CUDA-core path) or
+  // the chunk's S^T tiles fit their TMEM columns (tensor-core path); at most
+  // 1024 keys
+  int cmax = tc ? kTcMaxTiles * kTcTile : (kDecScoreBytes / 4 / gp) / kDecTile * kDecTile;
   if (cmax > 1024) cmax = 1024;
   // Enough CTAs to fill 4 per SM on 152 SMs where the keys allow chunks of at
   // least 256.
@@ -400,7 +703,7 @@ DecodePlan decode_plan(int B, int H, int Hkv, int N, int d) {
   if (nsplit < want) nsplit = want;
   if (nsplit < 1) nsplit = 1;
   long long chunk = (N + nsplit - 1) / nsplit;
-  chunk = (chunk + kDecTile - 1) / kDecTile * kDecTile;
+  chunk = (chunk + tile - 1) / tile * tile;
   DecodePlan p;
   p.chunk = static_cast<int>(chunk);
   p.nsplit = static_cast<int>((N + chunk - 1) / chunk);
@@ -415,6 +718,7 @@ size_t decode_workspace_bytes(int B, int H, int Hkv, int N, int d) {
 fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
   const DecodePlan p = decode_plan(a.B, a.H, a.Hkv, a.N, a.d);
   const int g = a.H / a.Hkv;
+  if (use_tc(g, a.d)) return launch_decode_tc(a, p, s);
   if (a.d == 64) {
     switch (g) {
       case 1: return launch_decode_impl<64, 1>(a, p, s);
