@@ -383,7 +383,7 @@ fa_status launch_decode_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStre
 
 
 // ---------------------------------------------------------------------------
-// Grouped heads (4..16 query heads per key/value head, d = 128): the score and
+// Grouped heads (2..16 query heads per key/value head, d = 128): the score and
 // P.V products are real contractions over the group, (keys x d)(d x heads)
 // and (d x keys)(keys x heads), so they go to the tensor cores, which leaves
 // the kernel bound by the cache read again.
@@ -679,7 +679,7 @@ fa_status launch_decode_tc(const DecodeArgs& a, const DecodePlan& pl, cudaStream
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-bool use_tc(int g, int d) { return d == 128 && g >= 4; }
+bool use_tc(int g, int d) { return d == 128 && g >= 2; }
 
 }  // namespace
 

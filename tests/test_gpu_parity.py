@@ -455,7 +455,7 @@ def _decode_case(B, H, Hkv, N, d, seed):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("N", [1, 63, 64, 1000, 5000])
-@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (6, 2), (16, 1)])
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (8, 2), (6, 2), (16, 1)])
 def test_decode_matches_oracle(d, N, H, Hkv):
     B = 2
     q, k, v = _decode_case(B, H, Hkv, N, d, seed=N + H)
