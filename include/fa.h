@@ -143,8 +143,9 @@ fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, 
  *   descale_q, descale_k, descale_v : DEVICE pointers to one fp32 each (delta).
  *   o   : [B,H,N,d] bf16 out, O = softmax(scale * (dq dk) q8 k8^T) (dv v8).
  *   lse : [B,H,N] fp32 out, natural-log LogSumExp of the scaled logits.
- * Inside, P is stored as e4m3 times 2^8 for the second product (P <= 2^0.75,
- * so P * 2^8 stays below 448); the factor is removed in the final division
+ * Inside, P is stored as e4m3 times 2^4 for the second product (the running
+ * maximum is raised whenever P would pass 2^4, so P * 2^4 stays at or below
+ * 256 < 448); the factor is removed in the final division
  * by the row sum.
  */
 fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale_q,
@@ -206,7 +207,7 @@ fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void*
  *   o, lse, B, H, N, causal, scale, stream : as fa_fwd_fp8.
  * S for query block i and key block j is scale * dq_i dk_j q8 k8^T.  V's
  * block scale is applied to P's e4m3 operand relative to the largest V scale
- * of the head (P * 2^8 * dv_j / max dv, never above 448), and O is multiplied
+ * of the head (P * 2^4 * dv_j / max dv, never above 448), and O is multiplied
  * by that largest scale at the end.  Where V's block scales differ, small P
  * values lose e4m3 precision; passing one V scale per head (the same value in
  * every block of descale_v) avoids that.
