@@ -4,8 +4,11 @@
 // differently from the forward over whole sequences; the row it computes is the
 // standard attention of "FLASH-ATTN", FlashAttention-2 > Background).
 //
-// The work is reading K and V once, so the kernel is organised for HBM
-// bandwidth, not for the tensor cores:
+// The work is reading K and V once, so the kernels are organised for HBM
+// bandwidth.  With one query head per key/value head (below) the products
+// are dot products and P.V on the FMA pipes; with 2..16 query heads sharing a
+// key/value head they are small contractions over the group and run on the
+// tensor cores (fa_decode_tc_kernel, further down).  The CUDA-core kernel:
 //  * the keys of one key/value head are cut into chunks; one CTA takes one
 //    chunk for all the query heads that share that key/value head (grouped
 //    queries read the cache once), and enough chunks exist to fill the GPU;
@@ -80,8 +83,9 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
 }
 
 // grid (nsplit, B*Hkv); each CTA: keys [chunk*C, min(N, chunk*C + C)) of one
-// key/value head, for its g query heads.  G: g fixed at compile time (1, 2, 4,
-// 8), or 16 for any g up to 16 read at run time.
+// key/value head, for its g query heads.  G: g fixed at compile time, or 16
+// for any g up to 16 read at run time; launched for g = 1 (grouped heads go to
+// the tensor-core kernel below, which measured faster from g = 2).
 template <int D, int G>
 __global__ void __launch_bounds__(kDecThreads, 3)
     fa_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -383,7 +387,7 @@ fa_status launch_decode_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStre
 
 
 // ---------------------------------------------------------------------------
-// Grouped heads (2..16 query heads per key/value head, d = 128): the score and
+// Grouped heads (2..16 query heads per key/value head): the score and
 // P.V products are real contractions over the group, (keys x d)(d x heads)
 // and (d x keys)(keys x heads), so they go to the tensor cores, which leaves
 // the kernel bound by the cache read again.
@@ -394,12 +398,14 @@ fa_status launch_decode_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStre
 //   warp 4    : TMA producer (K tiles, then V tiles, 3-slot ring).
 //   warp 5    : TMEM allocation and the MMA-issuing thread.
 // S^T = K Q^T (M = 128 keys, N = 16 padded heads, A = K tile K-major, B = Q
-// K-major) in TMEM columns 16 t; O^T += V^T P^T (M = d, N = 16, A = V tile
-// read MN-major, B = P K-major) in columns 128.. .
+// K-major) in TMEM columns 16 t; O^T += V^T P^T (M = 128 rows of d, N = 16,
+// A = V tile read MN-major, B = P K-major) in columns 128.. .  At d = 64 a
+// ring slot keeps its 128-row size: the product's rows 64..127 read the
+// slot's unused second half and are never read back.
 constexpr int kTcThreads = 192;
 constexpr int kTcTile = 128;           // keys per tile
 constexpr int kTcSlots = 3;
-constexpr int kTcTileBytes = kTcTile * 128 * 2;  // 32 KB (d = 128)
+constexpr int kTcTileBytes = kTcTile * 128 * 2;  // 32 KB: a 128-key tile at d = 128 (slot size)
 constexpr int kTcBlockBytes = kTcTile * 128;     // one 64-column block of a tile
 constexpr int kTcMaxTiles = 8;         // chunk <= 1024 keys
 constexpr int kTcN = 16;               // padded heads
@@ -429,6 +435,7 @@ __device__ __forceinline__ int kmaj_off(int r, int e, int rows) {
   return (e >> 6) * rows * 128 + r * 128 + ((((e & 63) >> 3) ^ (r & 7)) << 4) + ((e & 7) << 1);
 }
 
+template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fa_decode_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                         const __nv_bfloat16* __restrict__ q, float* __restrict__ part, int H, int Hkv, int N, int C,
@@ -467,9 +474,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_barrier_init();
   }
   // Q of the group as a 16-row K-major bf16 tile (rows past g are zero).
-  for (int i = t; i < kTcN * 128; i += kTcThreads) {
-    const int h = i >> 7, e = i & 127;
-    const __nv_bfloat16 val = h < g ? q[static_cast<size_t>(bq0 + h) * 128 + e] : __float2bfloat16_rn(0.f);
+  for (int i = t; i < kTcN * D; i += kTcThreads) {
+    const int h = i / D, e = i % D;
+    const __nv_bfloat16 val = h < g ? q[static_cast<size_t>(bq0 + h) * D + e] : __float2bfloat16_rn(0.f);
     *reinterpret_cast<__nv_bfloat16*>(s_qp + kmaj_off(h, e, kTcN)) = val;
   }
   fence_proxy_async_smem();  // generic-proxy stores -> tensor core reads
@@ -491,8 +498,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (round > 0 && !mbar_wait<true>(&sh.empty[slot], (round - 1) & 1, &sh.abort, &g_err_dec)) break;
         const bool is_k = it < n_tiles;
         const int key0 = key_begin + (is_k ? it : it - n_tiles) * kTcTile;
-        mbar_arrive_expect_tx(&sh.full[slot], kTcTileBytes);
-        for (int cb = 0; cb < 2; ++cb)
+        mbar_arrive_expect_tx(&sh.full[slot], kTcTile * D * 2);
+        for (int cb = 0; cb < D / 64; ++cb)
           tma_load_3d(s_ring + slot * kTcTileBytes + cb * kTcBlockBytes, is_k ? &map_k : &map_v, cb * 64, key0, bkv,
                       &sh.full[slot]);
         ++issued;
@@ -523,7 +530,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         const uint64_t a0 = sdesc_advance(ring_k, slot * kTcTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           mma_bf16_ss(tmem + tile * kTcN, sdesc_advance(a0, (kk >> 2) * kTcBlockBytes + (kk & 3) * 32),
                       sdesc_advance(q_k, (kk >> 2) * (kTcN * 128) + (kk & 3) * 32), kIdS, kk > 0);
         }
@@ -638,15 +645,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t r[16];
       tmem_ld16(tmem + lane_base + kTcTmO, r);  // thread t: column d = t of O^T
       tmem_ld_wait(r);
-      const size_t stride = 128 + 4;
+      const size_t stride = D + 4;
 #pragma unroll
       for (int h = 0; h < kTcN; ++h) {
-        if (h < g) {
+        if (h < g && t < D) {
           float* row = part + (static_cast<size_t>(bq0 + h) * nsplit + chunk) * stride;
           row[t] = __uint_as_float(r[h]);
           if (t == 0) {
-            row[128] = sh.m[h];
-            row[129] = sh.l[h];
+            row[D] = sh.m[h];
+            row[D + 1] = sh.l[h];
           }
         }
       }
@@ -661,25 +668,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-fa_status launch_decode_tc(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
+template <int D>
+fa_status launch_decode_tc_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
   CUtensorMap mk, mv;
   const int BHkv = a.B * a.Hkv;
-  if (!encode_rows_map(&mk, a.k, 2, 128, a.N, BHkv, 64, kTcTile) ||
-      !encode_rows_map(&mv, a.v, 2, 128, a.N, BHkv, 64, kTcTile))
+  if (!encode_rows_map(&mk, a.k, 2, D, a.N, BHkv, 64, kTcTile) ||
+      !encode_rows_map(&mv, a.v, 2, D, a.N, BHkv, 64, kTcTile))
     return FA_ERR_LAUNCH;
-  if (cudaFuncSetAttribute(fa_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
+  auto kern = fa_decode_tc_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
     return FA_ERR_LAUNCH;
   const dim3 grid(static_cast<unsigned>(pl.nsplit), static_cast<unsigned>(BHkv));
-  fa_decode_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.q), a.part,
-                                                         a.H, a.Hkv, a.N, pl.chunk, pl.nsplit,
-                                                         a.scale * 1.4426950408889634f);
+  kern<<<grid, kTcThreads, kTcSmem, s>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.q), a.part, a.H, a.Hkv, a.N,
+                                         pl.chunk, pl.nsplit, a.scale * 1.4426950408889634f);
   const int rows = a.B * a.H;
-  fa_decode_merge_kernel<128><<<(rows + 7) / 8, 256, 0, s>>>(a.part, static_cast<__nv_bfloat16*>(a.o), a.lse, rows,
-                                                            pl.nsplit);
+  fa_decode_merge_kernel<D><<<(rows + 7) / 8, 256, 0, s>>>(a.part, static_cast<__nv_bfloat16*>(a.o), a.lse, rows,
+                                                          pl.nsplit);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-bool use_tc(int g, int d) { return d == 128 && g >= 2; }
+fa_status launch_decode_tc(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
+  return a.d == 64 ? launch_decode_tc_impl<64>(a, pl, s) : launch_decode_tc_impl<128>(a, pl, s);
+}
+
+bool use_tc(int g, int d) { return g >= 2 && (d == 64 || d == 128); }
 
 }  // namespace
 
@@ -719,22 +731,8 @@ fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
   const DecodePlan p = decode_plan(a.B, a.H, a.Hkv, a.N, a.d);
   const int g = a.H / a.Hkv;
   if (use_tc(g, a.d)) return launch_decode_tc(a, p, s);
-  if (a.d == 64) {
-    switch (g) {
-      case 1: return launch_decode_impl<64, 1>(a, p, s);
-      case 2: return launch_decode_impl<64, 2>(a, p, s);
-      case 4: return launch_decode_impl<64, 4>(a, p, s);
-      case 8: return launch_decode_impl<64, 8>(a, p, s);
-      default: return launch_decode_impl<64, 16>(a, p, s);
-    }
-  }
-  switch (g) {
-    case 1: return launch_decode_impl<128, 1>(a, p, s);
-    case 2: return launch_decode_impl<128, 2>(a, p, s);
-    case 4: return launch_decode_impl<128, 4>(a, p, s);
-    case 8: return launch_decode_impl<128, 8>(a, p, s);
-    default: return launch_decode_impl<128, 16>(a, p, s);
-  }
+  // one query head per key/value head: the CUDA-core kernel
+  return a.d == 64 ? launch_decode_impl<64, 1>(a, p, s) : launch_decode_impl<128, 1>(a, p, s);
 }
 
 uint32_t decode_take_error(cudaStream_t s) {
