@@ -23,16 +23,18 @@
 //     diagonal block applies the element mask.
 //  3. fa_bwd_dq_convert: dQ = bf16(scale * dQ_acc).  HBM bound.
 //
-// Roles of fa_bwd_main_kernel (320 threads):
-//  warps 0-3  thread r owns key row r: P^T = exp2(S^T c - L_i log2 e) into
-//             TMEM (bf16, over S^T), then dS^T = P^T o (dP^T - D_i) into smem;
-//             finally writes dV.
+// Roles of fa_bwd_main_kernel (512 threads, four warpgroups):
+//  warps 0-3  thread r owns key row r for queries 0-63 of the block:
+//             P^T = exp2(S^T c - L_i log2 e) into TMEM (bf16, over S^T), then
+//             dS^T = P^T o (dP^T - D_i) into smem; finally half of dV.
+//  warps 12-15 the same for queries 64-127 and the other half of dV.
 //  warps 4-7  thread r owns query row r of the current block: reads dQ_i
 //             from TMEM and adds it into the fp32 accumulator; finally
 //             writes dK = scale * acc.
 //  warp 8     TMA producer: K and V once, Q_i and dO_i into two stages, and
 //             L_i, D_i into shared memory.
 //  warp 9     TMEM allocation and the single MMA-issuing thread.
+//  warps 10-11 no role (they complete the TMA/MMA warpgroup).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -46,7 +48,11 @@ namespace {
 
 __device__ uint32_t g_err_bwd;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 512;
+// Registers per thread at launch: 512 threads leave 128 each.  The launcher
+// checks that the compiled kernel uses exactly this many, because the
+// setmaxnreg split below must add up to the launch allocation.
+constexpr int kRegLaunch = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- preprocess
@@ -131,6 +137,15 @@ struct BwdCfg {
   static constexpr uint32_t kIdescKM = idesc_bf16(128, D, false, true);
   static constexpr uint32_t kIdescMM = idesc_bf16(128, D, true, true);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // Registers per thread after the warpgroups' setmaxnreg: at d = 128 the dQ
+  // warpgroup holds a whole 128-column fp32 dQ row, so it takes registers from
+  // the key-row and TMA/MMA warpgroups; the four shares add up to the launch
+  // allocation (a larger sum would leave the increase waiting forever).
+  static constexpr bool kRegSplit = (D == 128);
+  static constexpr int kRegKeyRow = kRegSplit ? 120 : kRegLaunch;
+  static constexpr int kRegCtl = kRegSplit ? 96 : kRegLaunch;
+  static constexpr int kRegDq = kRegSplit ? 176 : kRegLaunch;
+  static_assert(2 * kRegKeyRow + kRegCtl + kRegDq == 4 * kRegLaunch, "register split");
 };
 
 struct BwdBars {
@@ -226,14 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.q_full[s], 1);
       mbar_init(&sh.q_empty[s], 1);
       mbar_init(&sh.ld_full[s], 32);
-      mbar_init(&sh.ld_empty[s], 128);
+      mbar_init(&sh.ld_empty[s], 256);
     }
     mbar_init(&sh.do_full, 1);
     mbar_init(&sh.do_empty, 1);
     mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.p_ready, 128);
+    mbar_init(&sh.p_ready, 256);
     mbar_init(&sh.dp_full, 1);
-    mbar_init(&sh.ds_ready, 128);
+    mbar_init(&sh.ds_ready, 256);
     mbar_init(&sh.dv_done, 1);
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_free, 128);
@@ -247,180 +262,194 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    const int lane = lane_id();
-    if (lane == 0) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_do);
-      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kTileBytes);
-      for (int cb = 0; cb < C::kColBlocks; ++cb) {
-        tma_load_3d(smem + C::kOffK + cb * C::kBlockBytes, &map_k, cb * 64, kb * 128, bh, &sh.kv_full);
-        tma_load_3d(smem + C::kOffV + cb * C::kBlockBytes, &map_v, cb * 64, kb * 128, bh, &sh.kv_full);
-      }
-    }
-    int q_issued[2] = {0, 0};
-    int do_issued = 0;
-    QCursor cur{i_begin, qh0};
-    for (int it = 0; it < n_it; ++it) {
-      q_advance(cur, it);
-      if (__shfl_sync(0xffffffffu, sh.abort.flag, 0)) break;  // one decision for the whole warp
-      const int st = it & 1;
-      const int use = it >> 1;
-      const int qrow0 = cur.i * 128;
-      const int qh = cur.h;
-      bool ok = true;
+  if (warp >= 8 && warp < 12) {
+    // TMA/MMA warpgroup: warp 8 loads, warp 9 issues the products, warps 10
+    // and 11 have no role.
+    if constexpr (C::kRegSplit) setmaxnreg_dec<C::kRegCtl>();
+    if (warp == 8) {
+      // ------------------------------------------------------------ producer
+      const int lane = lane_id();
       if (lane == 0) {
-        // Q_i: two stages, freed when dK_(i-2) has read it.
-        if (use > 0) ok = mbar_wait(&sh.q_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd);
-        if (ok) {
-          mbar_arrive_expect_tx(&sh.q_full[st], C::kTileBytes);
-          for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * 64, qrow0, qh,
-                        &sh.q_full[st]);
-          ++q_issued[st];
-        }
-        // dO_i: one stage, freed when dV_(i-1) has read it.
-        if (ok && it > 0) ok = mbar_wait(&sh.do_empty, (it - 1) & 1, &sh.abort, &g_err_bwd);
-        if (ok) {
-          mbar_arrive_expect_tx(&sh.do_full, C::kTileBytes);
-          for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(smem + C::kOffDO + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, qh, &sh.do_full);
-          ++do_issued;
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_do);
+        mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kTileBytes);
+        for (int cb = 0; cb < C::kColBlocks; ++cb) {
+          tma_load_3d(smem + C::kOffK + cb * C::kBlockBytes, &map_k, cb * 64, kb * 128, bh, &sh.kv_full);
+          tma_load_3d(smem + C::kOffV + cb * C::kBlockBytes, &map_v, cb * 64, kb * 128, bh, &sh.kv_full);
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      if (use > 0 && !mbar_wait(&sh.ld_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd)) break;
-      // L in log2 units (+inf past the end: P = 0 there) and D, 4 rows per lane.
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int r = lane * 4 + u;
-        const int qg = qrow0 + r;
-        float l2 = -INFINITY, dd = -0.f;  // stored negated: -L log2 e and -D
-        if (qg < N) {
-          l2 = __ldg(lse + static_cast<size_t>(qh) * N + qg) * -kLog2e;
-          dd = -__ldg(dvec + static_cast<size_t>(qh) * N + qg);
-        }
-        s_lse2[st * 128 + r] = l2;
-        s_dvec[st * 128 + r] = dd;
-      }
-      mbar_arrive(&sh.ld_full[st]);
-    }
-    if (lane == 0 && sh.abort.flag) {
-      // Let every copy still in flight land before the CTA's memory goes away.
-      mbar_wait_drain(&sh.kv_full, 0, &g_err_bwd);
-      for (int s2 = 0; s2 < 2; ++s2)
-        if (q_issued[s2] > 0) mbar_wait_drain(&sh.q_full[s2], (q_issued[s2] - 1) & 1, &g_err_bwd);
-      if (do_issued > 0) mbar_wait_drain(&sh.do_full, (do_issued - 1) & 1, &g_err_bwd);
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    // Per query block i the five products are issued as
-    //   dV_i, S_(i+1), dK_i, dQ_i, dP_(i+1)
-    // so the key-row warpgroup computes P_(i+1) while dK_i and dQ_i run.
-    if (elect_one()) {
-      const uint32_t sm = smem_u32(smem);
-      // Base descriptors (K-major "_k", MN-major "_mn"); operands below advance
-      // them by byte offsets that are compile-time constants after unrolling.
-      const uint64_t k_k = sdesc_sw128(sm + C::kOffK, 16, 1024), k_mn = sdesc_sw128(sm + C::kOffK, C::kBlockBytes, 1024);
-      const uint64_t v_k = sdesc_sw128(sm + C::kOffV, 16, 1024);
-      const uint64_t ds_k = sdesc_sw128(sm + C::kOffDS, 16, 1024), ds_mn = sdesc_sw128(sm + C::kOffDS, C::kBlockBytes, 1024);
-      const uint64_t do_k = sdesc_sw128(sm + C::kOffDO, 16, 1024), do_mn = sdesc_sw128(sm + C::kOffDO, C::kBlockBytes, 1024);
-      const uint64_t q_k = sdesc_sw128(sm + C::kOffQ, 16, 1024), q_mn = sdesc_sw128(sm + C::kOffQ, C::kBlockBytes, 1024);
-      auto issue_s = [&](int i) {  // S^T = K Q_i^T
-        const uint64_t qb = sdesc_advance(q_k, (i & 1) * C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::kTmS, sdesc_advance(k_k, off), sdesc_advance(qb, off), C::kIdescKK, kk > 0);
-        }
-        tc_commit(&sh.s_full);
-      };
-      auto issue_dp = [&]() {  // dP^T = V dO_i^T
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::kTmDP, sdesc_advance(v_k, off), sdesc_advance(do_k, off), C::kIdescKK, kk > 0);
-        }
-        tc_commit(&sh.dp_full);
-      };
-      bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_err_bwd) &&
-                mbar_wait(&sh.q_full[0], 0, &sh.abort, &g_err_bwd);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        ok = mbar_wait(&sh.do_full, 0, &sh.abort, &g_err_bwd);
-        if (ok) {
-          tc_fence_after();
-          issue_dp();
-        }
-      }
-      for (int it = 0; ok && it < n_it; ++it) {
+      int q_issued[2] = {0, 0};
+      int do_issued = 0;
+      QCursor cur{i_begin, qh0};
+      for (int it = 0; it < n_it; ++it) {
+        q_advance(cur, it);
+        if (__shfl_sync(0xffffffffu, sh.abort.flag, 0)) break;  // one decision for the whole warp
         const int st = it & 1;
-        const uint64_t qm = sdesc_advance(q_mn, st * C::kTileBytes);
-        const bool has_next = it + 1 < n_it;
-        // dV += P_i^T dO_i
-        ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
+        const int use = it >> 1;
+        const int qrow0 = cur.i * 128;
+        const int qh = cur.h;
+        bool ok = true;
+        if (lane == 0) {
+          // Q_i: two stages, freed when dK_(i-2) has read it.
+          if (use > 0) ok = mbar_wait(&sh.q_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd);
+          if (ok) {
+            mbar_arrive_expect_tx(&sh.q_full[st], C::kTileBytes);
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_3d(smem + C::kOffQ + st * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * 64, qrow0, qh,
+                          &sh.q_full[st]);
+            ++q_issued[st];
+          }
+          // dO_i: one stage, freed when dV_(i-1) has read it.
+          if (ok && it > 0) ok = mbar_wait(&sh.do_empty, (it - 1) & 1, &sh.abort, &g_err_bwd);
+          if (ok) {
+            mbar_arrive_expect_tx(&sh.do_full, C::kTileBytes);
+            for (int cb = 0; cb < C::kColBlocks; ++cb)
+              tma_load_3d(smem + C::kOffDO + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, qh, &sh.do_full);
+            ++do_issued;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmS + kk * 8, sdesc_advance(do_mn, kk * 2048), C::kIdescKM,
-                      (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&sh.dv_done);
-        tc_commit(&sh.do_empty);
-        // S_(i+1): its columns hold P_i^T until dV_i has read them.
-        if (has_next) {
-          ok = mbar_wait(&sh.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, &sh.abort, &g_err_bwd) &&
-               mbar_wait(&sh.dv_done, it & 1, &sh.abort, &g_err_bwd);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(it + 1);
+        if (use > 0 && !mbar_wait(&sh.ld_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd)) break;
+        // L in log2 units (+inf past the end: P = 0 there) and D, 4 rows per lane.
+  #pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = lane * 4 + u;
+          const int qg = qrow0 + r;
+          float l2 = -INFINITY, dd = -0.f;  // stored negated: -L log2 e and -D
+          if (qg < N) {
+            l2 = __ldg(lse + static_cast<size_t>(qh) * N + qg) * -kLog2e;
+            dd = -__ldg(dvec + static_cast<size_t>(qh) * N + qg);
+          }
+          s_lse2[st * 128 + r] = l2;
+          s_dvec[st * 128 + r] = dd;
         }
-        // dK += dS_i^T Q_i ; dQ_i = dS_i K
-        ok = mbar_wait(&sh.ds_ready, it & 1, &sh.abort, &g_err_bwd);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::kTmDK, sdesc_advance(ds_k, off), sdesc_advance(qm, kk * 2048), C::kIdescKM,
-                      (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&sh.q_empty[st]);
-        if (D == 64 && it > 0) {  // separate dQ columns: only the previous read-out must be done
-          ok = mbar_wait(&sh.dq_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
-          if (!ok) break;
-          tc_fence_after();
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ss(tmem + C::kTmDQ, sdesc_advance(ds_mn, kk * 2048), sdesc_advance(k_mn, kk * 2048), C::kIdescMM,
-                      kk > 0);
-        tc_commit(&sh.dq_full);
-        // dP_(i+1)
-        if (has_next) {
-          ok = mbar_wait(&sh.do_full, (it + 1) & 1, &sh.abort, &g_err_bwd);
-          if (ok && D == 128)  // dP^T shares columns with dQ_i
-            ok = mbar_wait(&sh.dq_free, it & 1, &sh.abort, &g_err_bwd);
-          if (!ok) break;
-          tc_fence_after();
-          issue_dp();
-        }
+        mbar_arrive(&sh.ld_full[st]);
       }
-      if (ok) tc_commit(&sh.acc_done);
-      tc_commit(&sh.drain);
-      mbar_wait_drain(&sh.drain, 0, &g_err_bwd);
+      if (lane == 0 && sh.abort.flag) {
+        // Let every copy still in flight land before the CTA's memory goes away.
+        mbar_wait_drain(&sh.kv_full, 0, &g_err_bwd);
+        for (int s2 = 0; s2 < 2; ++s2)
+          if (q_issued[s2] > 0) mbar_wait_drain(&sh.q_full[s2], (q_issued[s2] - 1) & 1, &g_err_bwd);
+        if (do_issued > 0) mbar_wait_drain(&sh.do_full, (do_issued - 1) & 1, &g_err_bwd);
+      }
+      __syncwarp();
+    } else if (warp == 9) {
+      // ------------------------------------------------------------ MMA issuer
+      // Per query block i the five products are issued as
+      //   dV_i, S_(i+1), dK_i, dQ_i, dP_(i+1)
+      // so the key-row warpgroup computes P_(i+1) while dK_i and dQ_i run.
+      if (elect_one()) {
+        const uint32_t sm = smem_u32(smem);
+        // Base descriptors (K-major "_k", MN-major "_mn"); operands below advance
+        // them by byte offsets that are compile-time constants after unrolling.
+        const uint64_t k_k = sdesc_sw128(sm + C::kOffK, 16, 1024), k_mn = sdesc_sw128(sm + C::kOffK, C::kBlockBytes, 1024);
+        const uint64_t v_k = sdesc_sw128(sm + C::kOffV, 16, 1024);
+        const uint64_t ds_k = sdesc_sw128(sm + C::kOffDS, 16, 1024), ds_mn = sdesc_sw128(sm + C::kOffDS, C::kBlockBytes, 1024);
+        const uint64_t do_k = sdesc_sw128(sm + C::kOffDO, 16, 1024), do_mn = sdesc_sw128(sm + C::kOffDO, C::kBlockBytes, 1024);
+        const uint64_t q_k = sdesc_sw128(sm + C::kOffQ, 16, 1024), q_mn = sdesc_sw128(sm + C::kOffQ, C::kBlockBytes, 1024);
+        auto issue_s = [&](int i) {  // S^T = K Q_i^T
+          const uint64_t qb = sdesc_advance(q_k, (i & 1) * C::kTileBytes);
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+            mma_bf16_ss(tmem + C::kTmS, sdesc_advance(k_k, off), sdesc_advance(qb, off), C::kIdescKK, kk > 0);
+          }
+          tc_commit(&sh.s_full);
+        };
+        auto issue_dp = [&]() {  // dP^T = V dO_i^T
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+            mma_bf16_ss(tmem + C::kTmDP, sdesc_advance(v_k, off), sdesc_advance(do_k, off), C::kIdescKK, kk > 0);
+          }
+          tc_commit(&sh.dp_full);
+        };
+        bool ok = mbar_wait(&sh.kv_full, 0, &sh.abort, &g_err_bwd) &&
+                  mbar_wait(&sh.q_full[0], 0, &sh.abort, &g_err_bwd);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          ok = mbar_wait(&sh.do_full, 0, &sh.abort, &g_err_bwd);
+          if (ok) {
+            tc_fence_after();
+            issue_dp();
+          }
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int st = it & 1;
+          const uint64_t qm = sdesc_advance(q_mn, st * C::kTileBytes);
+          const bool has_next = it + 1 < n_it;
+          // dV += P_i^T dO_i
+          ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
+          if (!ok) break;
+          tc_fence_after();
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmS + kk * 8 + (kk >= 4 ? 64 : 0), sdesc_advance(do_mn, kk * 2048),
+                        C::kIdescKM,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&sh.dv_done);
+          tc_commit(&sh.do_empty);
+          // S_(i+1): its columns hold P_i^T until dV_i has read them.
+          if (has_next) {
+            ok = mbar_wait(&sh.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, &sh.abort, &g_err_bwd) &&
+                 mbar_wait(&sh.dv_done, it & 1, &sh.abort, &g_err_bwd);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(it + 1);
+          }
+          // dK += dS_i^T Q_i ; dQ_i = dS_i K
+          ok = mbar_wait(&sh.ds_ready, it & 1, &sh.abort, &g_err_bwd);
+          if (!ok) break;
+          tc_fence_after();
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+            mma_bf16_ss(tmem + C::kTmDK, sdesc_advance(ds_k, off), sdesc_advance(qm, kk * 2048), C::kIdescKM,
+                        (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&sh.q_empty[st]);
+          if (D == 64 && it > 0) {  // separate dQ columns: only the previous read-out must be done
+            ok = mbar_wait(&sh.dq_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
+            if (!ok) break;
+            tc_fence_after();
+          }
+  #pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C::kTmDQ, sdesc_advance(ds_mn, kk * 2048), sdesc_advance(k_mn, kk * 2048), C::kIdescMM,
+                        kk > 0);
+          tc_commit(&sh.dq_full);
+          // dP_(i+1)
+          if (has_next) {
+            ok = mbar_wait(&sh.do_full, (it + 1) & 1, &sh.abort, &g_err_bwd);
+            if (ok && D == 128)  // dP^T shares columns with dQ_i
+              ok = mbar_wait(&sh.dq_free, it & 1, &sh.abort, &g_err_bwd);
+            if (!ok) break;
+            tc_fence_after();
+            issue_dp();
+          }
+        }
+        if (ok) tc_commit(&sh.acc_done);
+        tc_commit(&sh.drain);
+        mbar_wait_drain(&sh.drain, 0, &g_err_bwd);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 4 || warp >= 12) {
     // ------------------------------------------------------------ P and dS (key rows)
-    const int r = threadIdx.x;  // key row within the block == TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // Two warpgroups share the key rows: warps 0-3 take queries 0-63 of the
+    // block, warps 12-15 queries 64-127 (a warp reaches the TMEM lanes of its
+    // own quarter, warp % 4).  P^T of the first half goes to S^T's columns
+    // 0-31 and of the second to columns 96-127, columns that each warpgroup
+    // has already read itself.
+    if constexpr (C::kRegSplit) setmaxnreg_dec<C::kRegKeyRow>();
+    const int half = warp >= 12 ? 1 : 0;
+    const int c0 = half * 64;  // first query of this warpgroup's half
+    const int r = static_cast<int>((warp & 3) * 32 + lane_id());  // key row within the block == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int kg = kb * 128 + r;
-    uint8_t* ds_row = smem + C::kOffDS + r * 128;
+    uint8_t* ds_row = smem + C::kOffDS + half * C::kBlockBytes + r * 128;
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     bool ok = true;
     QCursor cur{i_begin, qh0};
@@ -431,18 +460,18 @@ __global__ void __launch_bounds__(kThreads, 1)
            mbar_wait(&sh.s_full, it & 1, &sh.abort, &g_err_bwd);
       if (!ok) break;
       tc_fence_after();
-      const float* l2 = s_lse2 + st * 128;
-      const float* dd = s_dvec + st * 128;
+      const float* l2 = s_lse2 + st * 128 + c0;
+      const float* dd = s_dvec + st * 128 + c0;
       const bool diag = causal && (cur.i == kb);
       // window: query q of this block and key r are out of reach when
       // (query - key) >= window, i.e. dq0 + q - r >= window
       const int dq0 = (cur.i - kb) * 128;
       const bool wblk = WIN && dq0 + 127 >= window;
-      float p[128];
+      float p[64];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kTmS + cc * 32, rr);
+        tmem_ld32(tmem + lane_base + C::kTmS + c0 + cc * 32, rr);
         tmem_ld_wait(rr);
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {  // L for 4 queries per 16-byte broadcast load
@@ -456,18 +485,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float xv[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int q = cc * 32 + i + u;
-            if constexpr (WIN) p[q] = ((diag && q < r) || (wblk && dq0 + q - r >= window)) ? 0.f : xv[u];
-            else p[q] = (diag && q < r) ? 0.f : xv[u];  // query before key: masked
+            const int ql = cc * 32 + i + u;
+            const int q = c0 + ql;
+            if constexpr (WIN) p[ql] = ((diag && q < r) || (wblk && dq0 + q - r >= window)) ? 0.f : xv[u];
+            else p[ql] = (diag && q < r) ? 0.f : xv[u];  // query before key: masked
           }
         }
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      {
         uint32_t pw[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(p[64 * h + 2 * i], p[64 * h + 2 * i + 1]);
-        tmem_st32(tmem + lane_base + C::kTmS + h * 32, pw);
+        for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
+        tmem_st32(tmem + lane_base + C::kTmS + half * 96, pw);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -478,11 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kTmDP + cc * 32, rr);
+        tmem_ld32(tmem + lane_base + C::kTmDP + c0 + cc * 32, rr);
         tmem_ld_wait(rr);
-        // 32 queries = four 16-byte chunks of 8 in column block cc/2
+        // 32 queries = four 16-byte chunks of 8 in this half's column block
         uint32_t w[16];
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) {  // D for 4 queries per 16-byte broadcast load
@@ -497,11 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           w[2 * i2] = pack_bf16x2(a.x, a.y);
           w[2 * i2 + 1] = pack_bf16x2(b.x, b.y);
         }
-        uint8_t* blk = ds_row + (cc >> 1) * C::kBlockBytes;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + c4);
-          *reinterpret_cast<uint4*>(blk + ((chunk ^ swz) << 4)) =
+          const uint32_t chunk = static_cast<uint32_t>(cc * 4 + c4);
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ swz) << 4)) =
               make_uint4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
         }
       }
@@ -510,13 +538,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sh.ds_ready);
       mbar_arrive(&sh.ld_empty[st]);
     }
-    // dV = sum_i P_i^T dO_i
+    // dV = sum_i P_i^T dO_i, each warpgroup writing half of the columns
     if (ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd)) {
       tc_fence_after();
       const bool store = kg < N;
       __nv_bfloat16* dst = dv_out + (static_cast<size_t>(bh) * N + (store ? kg : 0)) * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D; cc += 32) {
+      for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
         uint32_t rr[32];
         tmem_ld32(tmem + lane_base + C::kTmDV + cc, rr);
         tmem_ld_wait(rr);
@@ -532,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ reduction (query rows), dK epilogue
+    if constexpr (C::kRegSplit) setmaxnreg_inc<C::kRegDq>();
     // dQ_i goes TMEM -> registers -> swizzled staging in shared memory ->
     // TMA reduce-add into the fp32 accumulator (the tensor map clips rows past N).
     const int r = threadIdx.x - 128;
@@ -633,6 +662,12 @@ fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   auto kern = fa_bwd_main_kernel<D, WIN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FA_ERR_LAUNCH;
+  if (C::kRegSplit) {
+    // The setmaxnreg shares assume the launch allocation; with any other
+    // count the dQ warpgroup's increase could never be granted.
+    cudaFuncAttributes fattr{};
+    if (cudaFuncGetAttributes(&fattr, kern) != cudaSuccess || fattr.numRegs != kRegLaunch) return FA_ERR_LAUNCH;
+  }
   const int n_blk = (a.N + 127) / 128;
   // Heads per group: Q, dO (bf16) and the dQ accumulator (fp32) of a group
   // should stay within about 48 MB of the L2.
