@@ -31,10 +31,10 @@
 //  warps 4-7  thread r owns query row r of the current block: reads dQ_i
 //             from TMEM and adds it into the fp32 accumulator; finally
 //             writes dK = scale * acc.
-//  warp 8     TMA producer: K and V once, Q_i and dO_i into two stages, and
-//             L_i, D_i into shared memory.
+//  warp 8     TMA producer: K and V once, Q_i into two stages, dO_i into one.
 //  warp 9     TMEM allocation and the single MMA-issuing thread.
-//  warps 10-11 no role (they complete the TMA/MMA warpgroup).
+//  warp 10    L_i and D_i of each query block into shared memory (two stages).
+//  warp 11    no role (it completes the TMA/MMA warpgroup).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sh.tmem_base;
 
   if (warp >= 8 && warp < 12) {
-    // TMA/MMA warpgroup: warp 8 loads, warp 9 issues the products, warps 10
-    // and 11 have no role.
+    // TMA/MMA warpgroup: warp 8 issues the tile copies, warp 9 the products,
+    // warp 10 loads L and D; warp 11 has no role.
     if constexpr (C::kRegSplit) setmaxnreg_dec<C::kRegCtl>();
     if (warp == 8) {
       // ------------------------------------------------------------ producer
@@ -310,21 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
-        if (use > 0 && !mbar_wait(&sh.ld_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd)) break;
-        // L in log2 units (+inf past the end: P = 0 there) and D, 4 rows per lane.
-  #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int r = lane * 4 + u;
-          const int qg = qrow0 + r;
-          float l2 = -INFINITY, dd = -0.f;  // stored negated: -L log2 e and -D
-          if (qg < N) {
-            l2 = __ldg(lse + static_cast<size_t>(qh) * N + qg) * -kLog2e;
-            dd = -__ldg(dvec + static_cast<size_t>(qh) * N + qg);
-          }
-          s_lse2[st * 128 + r] = l2;
-          s_dvec[st * 128 + r] = dd;
-        }
-        mbar_arrive(&sh.ld_full[st]);
       }
       if (lane == 0 && sh.abort.flag) {
         // Let every copy still in flight land before the CTA's memory goes away.
@@ -350,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t q_k = sdesc_sw128(sm + C::kOffQ, 16, 1024), q_mn = sdesc_sw128(sm + C::kOffQ, C::kBlockBytes, 1024);
         auto issue_s = [&](int i) {  // S^T = K Q_i^T
           const uint64_t qb = sdesc_advance(q_k, (i & 1) * C::kTileBytes);
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
             mma_bf16_ss(tmem + C::kTmS, sdesc_advance(k_k, off), sdesc_advance(qb, off), C::kIdescKK, kk > 0);
@@ -358,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(&sh.s_full);
         };
         auto issue_dp = [&]() {  // dP^T = V dO_i^T
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
             mma_bf16_ss(tmem + C::kTmDP, sdesc_advance(v_k, off), sdesc_advance(do_k, off), C::kIdescKK, kk > 0);
@@ -384,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
           if (!ok) break;
           tc_fence_after();
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmS + kk * 8 + (kk >= 4 ? 64 : 0), sdesc_advance(do_mn, kk * 2048),
                         C::kIdescKM,
@@ -403,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&sh.ds_ready, it & 1, &sh.abort, &g_err_bwd);
           if (!ok) break;
           tc_fence_after();
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
             mma_bf16_ss(tmem + C::kTmDK, sdesc_advance(ds_k, off), sdesc_advance(qm, kk * 2048), C::kIdescKM,
@@ -415,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
           }
-  #pragma unroll
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ss(tmem + C::kTmDQ, sdesc_advance(ds_mn, kk * 2048), sdesc_advance(k_mn, kk * 2048), C::kIdescMM,
                         kk > 0);
@@ -435,6 +420,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(&sh.drain, 0, &g_err_bwd);
       }
       __syncwarp();
+    } else if (warp == 10) {
+      // ------------------------------------------------------------ L and D rows
+      // L in log2 units (+inf past the end: P = 0 there) and D of each query
+      // block, two stages ahead of the key-row warpgroups, 4 rows per lane.
+      const int lane = lane_id();
+      QCursor cur{i_begin, qh0};
+      for (int it = 0; it < n_it; ++it) {
+        q_advance(cur, it);
+        const int st = it & 1;
+        const int use = it >> 1;
+        if (use > 0 && !mbar_wait(&sh.ld_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd)) break;
+        const int qrow0 = cur.i * 128;
+        const int qh = cur.h;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = lane * 4 + u;
+          const int qg = qrow0 + r;
+          float l2 = -INFINITY, dd = -0.f;  // stored negated: -L log2 e and -D
+          if (qg < N) {
+            l2 = __ldg(lse + static_cast<size_t>(qh) * N + qg) * -kLog2e;
+            dd = -__ldg(dvec + static_cast<size_t>(qh) * N + qg);
+          }
+          s_lse2[st * 128 + r] = l2;
+          s_dvec[st * 128 + r] = dd;
+        }
+        mbar_arrive(&sh.ld_full[st]);
+      }
     }
   } else if (warp < 4 || warp >= 12) {
     // ------------------------------------------------------------ P and dS (key rows)
