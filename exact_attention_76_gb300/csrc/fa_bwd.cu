@@ -114,8 +114,7 @@ struct BwdCfg {
   static constexpr int kColBlocks = D / 64;        // 128-byte column blocks per bf16 row
   static constexpr int kBlockBytes = 128 * 128;    // one 128-row x 128-byte block
   static constexpr int kDsBytes = 128 * 128 * 2;   // dS^T, 128 keys x 128 queries, bf16
-  static constexpr int kStageBytes = 32768;        // dQ staging: 2 blocks of 128 rows x 32 fp32
-  static constexpr int kDqRounds = (D * 4) / 256;  // dQ row = D fp32; 64 columns (2 blocks) per round
+  static constexpr int kStageBytes = 32768;        // dQ staging: 2 blocks of 128 rows x 32 fp32, used in turn
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
@@ -601,31 +600,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sh.dq_free);
       const int qrow0 = cur.i * 128;
       const int qh = cur.h;
+      // 32-column blocks (128 rows x 128 bytes, swizzled for the reduce-add)
+      // alternate between the two halves of the staging buffer, so that the
+      // rows of block b are written while block b-1 is still being read.
 #pragma unroll
-      for (int round = 0; round < C::kDqRounds; ++round) {
-        if (staged_before) {
-          if (leader) bulk_wait_read_all();  // the previous reduce has read the staging buffer
+      for (int b = 0; b < D / 32; ++b) {
+        if (staged_before || b >= 2) {
+          if (leader) bulk_wait_read_1();  // the reduce from this half (two blocks back) has read it
           named_bar_sync(1, 128);
         }
+        uint8_t* blk = stage_row + (b & 1) * C::kBlockBytes;
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {  // two 32-column blocks of 128 rows x 128 bytes
-          uint8_t* blk = stage_row + b * C::kBlockBytes;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int col = round * 64 + b * 32 + c * 4;
-            *reinterpret_cast<float4*>(blk + ((static_cast<uint32_t>(c) ^ swz) << 4)) =
-                make_float4(v[col], v[col + 1], v[col + 2], v[col + 3]);
-          }
+        for (int c = 0; c < 8; ++c) {
+          const int col = b * 32 + c * 4;
+          *reinterpret_cast<float4*>(blk + ((static_cast<uint32_t>(c) ^ swz) << 4)) =
+              make_float4(v[col], v[col + 1], v[col + 2], v[col + 3]);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (leader) {
-          tma_reduce_add_3d(&map_dq, round * 64, qrow0, qh, smem + C::kOffStage);
-          tma_reduce_add_3d(&map_dq, round * 64 + 32, qrow0, qh, smem + C::kOffStage + C::kBlockBytes);
+          tma_reduce_add_3d(&map_dq, b * 32, qrow0, qh, smem + C::kOffStage + (b & 1) * C::kBlockBytes);
           bulk_commit_group();
         }
-        staged_before = true;
       }
+      staged_before = true;
     }
     if (leader) bulk_wait_all();
     // dK = scale * sum_i dS_i^T Q_i
