@@ -132,6 +132,12 @@ struct BwdCfg {
   static constexpr uint32_t kTmS = 2 * D;
   static constexpr uint32_t kTmDP = 2 * D + 128;
   static constexpr uint32_t kTmDQ = (D == 128) ? kTmDP : 2 * D + 256;  // aliases dP^T when D = 128
+  // P^T (bf16 pairs, 64 columns): at d = 64 in the spare columns 448-511, so
+  // that S^T of the next block need not wait for dV to have read P; at d = 128
+  // over S^T (queries 0-63 in columns 0-31, 64-127 in 96-127).
+  static constexpr bool kOwnP = (D == 64);
+  static constexpr uint32_t kTmP = kOwnP ? 2 * D + 256 + 64 : kTmS;
+  static_assert(!kOwnP || kTmP + 64 <= 512, "TMEM columns");
   static constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t kIdescKM = idesc_bf16(128, D, false, true);
   static constexpr uint32_t kIdescMM = idesc_bf16(128, D, true, true);
@@ -370,15 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmS + kk * 8 + (kk >= 4 ? 64 : 0), sdesc_advance(do_mn, kk * 2048),
-                        C::kIdescKM,
-                        (it > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmP + kk * 8 + ((C::kOwnP || kk < 4) ? 0 : 64),
+                        sdesc_advance(do_mn, kk * 2048), C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&sh.dv_done);
           tc_commit(&sh.do_empty);
-          // S_(i+1): its columns hold P_i^T until dV_i has read them.
+          // S_(i+1): at d = 128 its columns hold P_i^T until dV_i has read them.
           if (has_next) {
             ok = mbar_wait(&sh.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, &sh.abort, &g_err_bwd) &&
-                 mbar_wait(&sh.dv_done, it & 1, &sh.abort, &g_err_bwd);
+                 (C::kOwnP || mbar_wait(&sh.dv_done, it & 1, &sh.abort, &g_err_bwd));
             if (!ok) break;
             tc_fence_after();
             issue_s(it + 1);
@@ -451,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ P and dS (key rows)
     // Two warpgroups share the key rows: warps 0-3 take queries 0-63 of the
     // block, warps 12-15 queries 64-127 (a warp reaches the TMEM lanes of its
-    // own quarter, warp % 4).  P^T of the first half goes to S^T's columns
-    // 0-31 and of the second to columns 96-127, columns that each warpgroup
-    // has already read itself.
+    // own quarter, warp % 4).  At d = 128, P^T of the first half goes to
+    // S^T's columns 0-31 and of the second to columns 96-127, columns that
+    // each warpgroup has already read itself; at d = 64 to columns of its own.
     if constexpr (C::kRegSplit) setmaxnreg_dec<C::kRegKeyRow>();
     const int half = warp >= 12 ? 1 : 0;
     const int c0 = half * 64;  // first query of this warpgroup's half
@@ -478,37 +483,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (query - key) >= window, i.e. dq0 + q - r >= window
       const int dq0 = (cur.i - kb) * 128;
       const bool wblk = WIN && dq0 + 127 >= window;
+      // P stays fp32 for dS and goes to TMEM as bf16 pairs for dV.
       float p[64];
+      uint32_t pw[32];
+      auto p_quad = [&](const uint32_t (&rr)[32], int cc, int i4, float (&pv)[4]) {
+        const float4 lq = reinterpret_cast<const float4*>(l2)[cc * 8 + i4];  // -L log2 e, 4 queries
+        const int i = i4 * 4;
+        const float2 c2 = make_float2(scale_log2, scale_log2);
+        const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])), c2,
+                                      make_float2(lq.x, lq.y));
+        const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])), c2,
+                                      make_float2(lq.z, lq.w));
+        const float xv[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kTmS + c0 + cc * 32, rr);
-        tmem_ld_wait(rr);
+        for (int u = 0; u < 4; ++u) {
+          const int q = c0 + cc * 32 + i + u;
+          if constexpr (WIN) pv[u] = ((diag && q < r) || (wblk && dq0 + q - r >= window)) ? 0.f : xv[u];
+          else pv[u] = (diag && q < r) ? 0.f : xv[u];  // query before key: masked
+        }
+      };
+      if constexpr (D == 64) {
+        // Both TMEM loads of S^T before one wait, P packed as it is made
+        // (measured +8 % at d = 64, slower at d = 128 with 120 registers).
+        uint32_t rs[2][32];
+        tmem_ld32(tmem + lane_base + C::kTmS + c0, rs[0]);
+        tmem_ld32(tmem + lane_base + C::kTmS + c0 + 32, rs[1]);
+        tmem_ld_wait(rs[0]);
+        tmem_ld_wait(rs[1]);
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {  // L for 4 queries per 16-byte broadcast load
-          const float4 lq = reinterpret_cast<const float4*>(l2)[cc * 8 + i4];  // -L log2 e
-          const int i = i4 * 4;
-          const float2 c2 = make_float2(scale_log2, scale_log2);
-          const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])), c2,
-                                        make_float2(lq.x, lq.y));
-          const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(rr[i + 2]), __uint_as_float(rr[i + 3])), c2,
-                                        make_float2(lq.z, lq.w));
-          const float xv[4] = {ex2_approx(x01.x), ex2_approx(x01.y), ex2_approx(x23.x), ex2_approx(x23.y)};
+        for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int ql = cc * 32 + i + u;
-            const int q = c0 + ql;
-            if constexpr (WIN) p[ql] = ((diag && q < r) || (wblk && dq0 + q - r >= window)) ? 0.f : xv[u];
-            else p[ql] = (diag && q < r) ? 0.f : xv[u];  // query before key: masked
+          for (int i4 = 0; i4 < 8; ++i4) {
+            float pv[4];
+            p_quad(rs[cc], cc, i4, pv);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) p[cc * 32 + i4 * 4 + u] = pv[u];
+            pw[cc * 16 + 2 * i4] = pack_bf16x2(pv[0], pv[1]);
+            pw[cc * 16 + 2 * i4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + C::kTmS + c0 + cc * 32, rr);
+          tmem_ld_wait(rr);
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            float pv[4];
+            p_quad(rr, cc, i4, pv);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) p[cc * 32 + i4 * 4 + u] = pv[u];
           }
         }
-      }
-      {
-        uint32_t pw[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-        tmem_st32(tmem + lane_base + C::kTmS + half * 96, pw);
       }
+      // (P_(i-1) there has been read: S_i, whose completion was awaited, was
+      // issued after dV_(i-1).)
+      tmem_st32(tmem + lane_base + C::kTmP + half * (C::kOwnP ? 32 : 96), pw);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sh.p_ready);
