@@ -25,7 +25,7 @@
 //
 // Roles of fa_bwd_main_kernel (512 threads, four warpgroups):
 //  warps 0-3  thread r owns key row r for queries 0-63 of the block:
-//             P^T = exp2(S^T c - L_i log2 e) into TMEM (bf16, over S^T), then
+//             P^T = exp2(S^T c - L_i log2 e) into TMEM (bf16; over S^T at d = 128), then
 //             dS^T = P^T o (dP^T - D_i) into smem; finally half of dV.
 //  warps 12-15 the same for queries 64-127 and the other half of dV.
 //  warps 4-7  thread r owns query row r of the current block: reads dQ_i
