@@ -502,9 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           else pv[u] = (diag && q < r) ? 0.f : xv[u];  // query before key: masked
         }
       };
-      if constexpr (D == 64) {
-        // Both TMEM loads of S^T before one wait, P packed as it is made
-        // (measured +8 % at d = 64, slower at d = 128 with 120 registers).
+      {
+        // Both TMEM loads of S^T before one wait (tcgen05.wait::ld waits for
+        // every outstanding load), P packed as it is made.
         uint32_t rs[2][32];
         tmem_ld32(tmem + lane_base + C::kTmS + c0, rs[0]);
         tmem_ld32(tmem + lane_base + C::kTmS + c0 + 32, rs[1]);
@@ -521,22 +521,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             pw[cc * 16 + 2 * i4] = pack_bf16x2(pv[0], pv[1]);
             pw[cc * 16 + 2 * i4 + 1] = pack_bf16x2(pv[2], pv[3]);
           }
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + lane_base + C::kTmS + c0 + cc * 32, rr);
-          tmem_ld_wait(rr);
-#pragma unroll
-          for (int i4 = 0; i4 < 8; ++i4) {
-            float pv[4];
-            p_quad(rr, cc, i4, pv);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) p[cc * 32 + i4 * 4 + u] = pv[u];
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pw[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
       }
       // (P_(i-1) there has been read: S_i, whose completion was awaited, was
       // issued after dV_(i-1).)
