@@ -145,6 +145,60 @@ def test_gqa_forward_backward(H, Hkv, N, d, causal):
         assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e}"
 
 
+# ---------------------------------------------------------------- more work items than SMs
+# More (query-tile pair, head) items than the GPU has SMs, of unequal length
+# under the causal mask and with idle second tiles in the last query block of
+# every head (ragged N): the cases a schedule that reuses CTAs across items
+# must get right, kept as parity cases for the block-per-item schedule.
+
+MANY_ITEMS = [
+    # (B, H, Hkv, N, d, causal): ceil(N / 256) * B * H items, all above 152
+    (4, 40, 40, 600, 64, True),
+    (2, 48, 12, 520, 128, False),
+    (2, 48, 48, 777, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal", MANY_ITEMS)
+def test_forward_backward_many_items(B, H, Hkv, N, d, causal):
+    q, _, _, do = inputs.draw_bf16(B, H, N, d, seed=N + H)
+    _, k, v, _ = inputs.draw_bf16(B, Hkv, N, d, seed=N + Hkv + 1)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    o, lse = api.fa_fwd_gqa(qd, kd, vd, causal, scale)
+    dq, dk, dv = api.fa_bwd_gqa(qd, kd, vd, o, lse, dod, causal, scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.forward_gqa(q, k, v, causal, scale)
+    assert max_abs(f64(o), o_ref) <= O_MAX_ABS
+    assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
+    for name, got, ref in zip(("dQ", "dK", "dV"), (dq, dk, dv), oracle.backward_gqa(q, k, v, do, causal, scale)):
+        e = rel_fro(f64(got), ref)
+        assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e}"
+
+
+def test_window_many_items():
+    B, H, N, d, window = 2, 40, 700, 128, 300  # 240 items
+    q, k, v, _ = inputs.draw_bf16(B, H, N, d, seed=window + 1)
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd = to_dev(q, k, v)
+    o, lse = api.fa_fwd_window(qd, kd, vd, window, scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.forward_window(q, k, v, window, scale)
+    assert np.all(np.abs(f64(o) - o_ref) <= np.maximum(O_MAX_ABS, o_rounding_bound(o_ref, v)))
+    assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_many_items(causal):
+    # 3 * 64 = 192 items; against exact attention on the dequantised inputs
+    orig, codes, deltas, o, lse, scale = _fp8_case(640, causal, B=1, H=64)
+    deq = [oracle.dequantize_e4m3(c, dl) for c, dl in zip(codes, deltas)]
+    o_deq, l_deq = oracle.forward(*deq, causal, scale)
+    e = rel_fro(f64(o), o_deq)
+    assert e <= FP8_O_REL_FRO, f"FP8 O rel-Frobenius vs dequantised inputs {e:.3e}"
+    assert max_abs(f64(lse), l_deq) <= 2e-2
+
+
 # ---------------------------------------------------------------- step by step
 
 def test_preprocess_and_convert_steps():
