@@ -436,6 +436,51 @@ def run_decode(args):
     return 0
 
 
+def run_fp8(args):
+    """FP8 e4m3 forward on the FP8 workload (a side measurement, not the bench's
+    workload): B=1, H=16, N=16384, d=128, Q, K, V drawn N(0,1) with 0.1 % of the
+    entries scaled by 10, stored as per-tensor e4m3 by the library's quantiser;
+    timed with CUDA events on the launching stream against the fp8 peak (the
+    measured bf16 figure times 2, the nominal fp8:bf16 ratio)."""
+    import torch
+
+    from exact_attention_76_gb300 import api, inputs
+    from exact_attention_76_gb300 import build as _build
+
+    _build.build()
+    causal = args.fp8 == "causal"
+    B, H, N, d = 1, 16, 16384, 128
+    q, k, v = (t.cuda() for t in inputs.draw_outlier_fp32(B, H, N, d, seed=5))
+    (q8, dq), (k8, dk), (v8, dv) = (api.fa_fp8_quantize(t, False) for t in (q, k, v))
+    del q, k, v
+    o = torch.empty(B, H, N, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 3)):
+        api.fa_fwd_fp8(q8, k8, v8, dq, dk, dv, causal, scale, o=o, lse=lse, stream=stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        api.fa_fwd_fp8(q8, k8, v8, dq, dk, dv, causal, scale, o=o, lse=lse, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    fl, _ = flops_step(B, H, N, d, causal)
+    tflops = fl / ms / 1e9
+    peaks, src = measured_peaks()
+    peak = 2.0 * peaks["bf16_tflops"]
+    print(json.dumps({"metric": "attention fwd TFLOPS (fp8 e4m3, per-tensor scales, d=128, 1xGB300)",
+                      "value": tflops, "unit": "TFLOP/s", "steps": args.steps, "ms_per_step": ms,
+                      "higher_is_better": True, "dtype": "e4m3", "data": "synthetic",
+                      "config": {"workload": f"fp8_B{B}_H{H}_N{N}_d{d}_{args.fp8}"},
+                      "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                                   "frac": tflops / peak, "peak_source": src + " bf16 burst x 2 (fp8:bf16)"}}),
+          flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,9 +492,13 @@ def main():
     ap.add_argument("--shape", default="", help="B,H,N,d of a causal profiling case instead of the workload")
     ap.add_argument("--decode", default="", help="B,H,Hkv,N,d: time fa_decode instead (side measurement)")
     ap.add_argument("--mufu", action="store_true", help="measure the special-function unit's exp2 rate")
+    ap.add_argument("--fp8", choices=["full", "causal"], default="",
+                    help="time the FP8 forward on B=1 H=16 N=16384 d=128 instead (side measurement)")
     args = ap.parse_args()
     if args.decode:
         return run_decode(args)
+    if args.fp8:
+        return run_fp8(args)
     if args.mufu:
         from exact_attention_76_gb300 import api
         from exact_attention_76_gb300 import build as _build
