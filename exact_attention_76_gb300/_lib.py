@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
 
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
-                4: "FA_ERR_LAUNCH", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_WORKSPACE"}
+                4: "FA_ERR_LAUNCH", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_KERNEL_CONFIG"}
 
 # (name, argtypes, restype) for every symbol include/fa.h declares.
 _P, _I, _F, _Z, _U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint
@@ -39,7 +39,9 @@ SIGNATURES = {
     "fa_fp8_quantize_blocks": ([_P, _I, _I, _I, _P, _P, _I, _I, _I, _P], _I),
     "fa_fwd_window": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P], _I),
     "fa_bwd_window": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _I, _F, _P], _I),
-    "fa_measure_ex2_rate": ([_P, _P], _I),
+    "fa_measure_ex2_rate_scratch_size": ([], _Z),
+    "fa_measure_ex2_rate": ([_P, _P, _Z, _P], _I),
+    "fa_debug_exp2_poly": ([_P, _P, _L, _I, _P], _I),
     "fa_decode_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "fa_decode": ([_P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _F, _P], _I),
 }

@@ -314,11 +314,29 @@ def fa_decode(q, k, v, scale: float, o=None, lse=None, workspace=None, stream=No
 
 
 def fa_measure_ex2_rate(stream=None) -> float:
-    """exp2 results per clock per SM of the special-function unit (a measurement)."""
+    """exp2 results per clock per SM of the special-function unit (a measurement;
+    synchronises the stream).  Its scratch is allocated here with torch."""
     import ctypes
+    lib = _lib.load()
+    nbytes = int(lib.fa_measure_ex2_rate_scratch_size())
+    if nbytes == 0:
+        raise RuntimeError("fa_measure_ex2_rate_scratch_size: no current CUDA device")
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     out = ctypes.c_float(0.0)
-    _lib.check("fa_measure_ex2_rate", _lib.load().fa_measure_ex2_rate(ctypes.byref(out), _stream_ptr(stream)))
+    _lib.check("fa_measure_ex2_rate", lib.fa_measure_ex2_rate(ctypes.byref(out), _ptr(scratch), nbytes,
+                                                               _stream_ptr(stream)))
     return float(out.value)
+
+
+def fa_debug_exp2_poly(x, degree: int, y=None, stream=None):
+    """2^x by the library's FMA-pipe polynomial (test hook); x fp32 CUDA."""
+    lib = _lib.load()
+    _check(x, "x", torch.float32)
+    y = torch.empty_like(x) if y is None else y
+    _check(y, "y", torch.float32, tuple(x.shape))
+    _lib.check("fa_debug_exp2_poly", lib.fa_debug_exp2_poly(_ptr(x), _ptr(y), x.numel(), int(degree),
+                                                             _stream_ptr(stream)))
+    return y
 
 
 def fa_status_string(status: int) -> str:

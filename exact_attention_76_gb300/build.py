@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -21,6 +22,10 @@ LIB = os.path.join(HERE, "libfa_gb300.so")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu", "fa_fp8q.cu", "fa_decode.cu"]
 HEADERS = ["fa_common.cuh", "fa_host.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Kernels whose warpgroups redistribute registers with setmaxnreg: the shares
+# add up to the launch allocation only if the compiled kernel uses exactly
+# this many registers per thread (source, mangled-name fragment, registers).
+REGISTER_PLANS = [("fa_bwd.cu", "fa_bwd_main_kernelILi128E", 128)]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
 
@@ -46,6 +51,28 @@ def stale() -> bool:
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
+def check_registers(ptxas_log: str, fragment: str, regs: int, src: str) -> None:
+    """Fails the build unless every kernel whose mangled name contains
+    `fragment` was compiled to exactly `regs` registers per thread (ptxas -v:
+    an entry function line, then its "Used N registers" line)."""
+    found = 0
+    current = None
+    for line in ptxas_log.splitlines():
+        m = re.search(r"Compiling entry function '([^']+)'", line)
+        if m:
+            current = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and current is not None and fragment in current:
+            found += 1
+            if int(m.group(1)) != regs:
+                raise RuntimeError(f"{src}: {current} uses {m.group(1)} registers per thread; its setmaxnreg "
+                                   f"split needs exactly {regs}")
+            current = None
+    if found == 0:
+        raise RuntimeError(f"{src}: no register report for a kernel matching {fragment}")
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     if not force and not stale():
         return LIB
@@ -55,11 +82,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+        plans = [pl for pl in REGISTER_PLANS if pl[0] == src]
+        flags = extra if (extra or not plans) else ["-Xptxas", "-v"]
+        cmd = [cc, *ARCH, *FLAGS, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{p.stderr}")
-        return obj, p.stderr
+        for _, frag, regs in plans:
+            check_registers(p.stderr, frag, regs, src)
+        return obj, p.stderr if (verbose or ptxas_info) else ""
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))

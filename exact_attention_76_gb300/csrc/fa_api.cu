@@ -134,6 +134,36 @@ fa_status launch_ex2_rate(int blocks, int iters, float* sink, long long* cycles,
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// The polynomial exp2 of fa_common.cuh over an array (test hook): each thread
+// takes two elements, the packed pair the kernels evaluate it on.
+template <int DEG>
+__global__ void __launch_bounds__(256) exp2_poly_kernel(const float* __restrict__ x, float* __restrict__ y,
+                                                        long long n) {
+  const long long i = 2 * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x1 = i + 1 < n ? x[i + 1] : 0.0f;
+  const float2 r = exp2_poly2<DEG>(make_float2(x[i], x1));
+  y[i] = r.x;
+  if (i + 1 < n) y[i + 1] = r.y;
+}
+
+fa_status launch_exp2_poly(const float* x, float* y, long long n, int degree, cudaStream_t stream) {
+  const long long blocks = (n + 511) / 512;
+  if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  if (degree == 2)
+    exp2_poly_kernel<2><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, y, n);
+  else
+    exp2_poly_kernel<3><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, y, n);
+  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+// Scratch of the exp2-rate measurement: the sink (one float per thread) and
+// one cycle count per CTA, for two CTAs of 512 threads per SM.
+size_t ex2_rate_scratch_bytes(int sms) {
+  const size_t blocks = 2 * static_cast<size_t>(sms);
+  return round16(blocks * 512 * sizeof(float)) + blocks * sizeof(long long);
+}
+
 fa_status launch_timeout_probe(unsigned int limit_us, cudaStream_t stream) {
   int dev = 0, khz = 2000000;
   cudaGetDevice(&dev);
@@ -368,6 +398,8 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: kernel launch or tensor-map encoding failed";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait ran past its limit";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+    case FA_ERR_KERNEL_CONFIG:
+      return "FA_ERR_KERNEL_CONFIG: the compiled kernel's register count differs from its launch plan";
   }
   return "unknown fa_status";
 }
@@ -382,23 +414,28 @@ fa_status fa_device_error(void* stream) {
   return FA_OK;
 }
 
-fa_status fa_measure_ex2_rate(float* ex2_per_clock_per_sm, void* stream) {
+size_t fa_measure_ex2_rate_scratch_size(void) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 0;
+  return ex2_rate_scratch_bytes(sms);
+}
+
+fa_status fa_measure_ex2_rate(float* ex2_per_clock_per_sm, void* scratch, size_t scratch_bytes, void* stream) {
   fa_status st;
-  if (ex2_per_clock_per_sm == nullptr) return FA_ERR_INVALID_ARG;
+  if (ex2_per_clock_per_sm == nullptr || scratch == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned16(scratch)) return FA_ERR_ALIGNMENT;
   if ((st = check_device()) != FA_OK) return st;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0 || scratch_bytes < ex2_rate_scratch_bytes(sms)) return FA_ERR_WORKSPACE;
   const int blocks = 2 * sms, iters = 4096;  // two CTAs of 512 threads per SM
-  float* sink = nullptr;
-  long long* cycles = nullptr;
+  float* sink = static_cast<float*>(scratch);
+  long long* cycles = reinterpret_cast<long long*>(static_cast<char*>(scratch) +
+                                                   round16(static_cast<size_t>(blocks) * 512 * sizeof(float)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMallocAsync(reinterpret_cast<void**>(&sink), sizeof(float) * blocks * 512, s) != cudaSuccess)
-    return FA_ERR_LAUNCH;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&cycles), sizeof(long long) * blocks, s) != cudaSuccess) {
-    cudaFreeAsync(sink, s);
-    return FA_ERR_LAUNCH;
-  }
   st = launch_ex2_rate(blocks, iters, sink, cycles, s);  // warm-up
   if (st == FA_OK) st = launch_ex2_rate(blocks, iters, sink, cycles, s);
   long long* host = new long long[blocks];
@@ -413,10 +450,15 @@ fa_status fa_measure_ex2_rate(float* ex2_per_clock_per_sm, void* stream) {
     *ex2_per_clock_per_sm = static_cast<float>(2.0 * 512.0 * 8.0 * iters / static_cast<double>(worst));
   }
   delete[] host;
-  cudaFreeAsync(sink, s);
-  cudaFreeAsync(cycles, s);
-  cudaStreamSynchronize(s);
   return st;
+}
+
+fa_status fa_debug_exp2_poly(const float* x, float* y, long long n, int degree, void* stream) {
+  fa_status st;
+  if ((st = check_ptrs(x, y)) != FA_OK) return st;
+  if (n <= 0 || (degree != 2 && degree != 3)) return FA_ERR_INVALID_ARG;
+  if ((st = check_device()) != FA_OK) return st;
+  return launch_exp2_poly(x, y, n, degree, static_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_debug_wait_timeout(unsigned int limit_us, void* stream) {

@@ -49,8 +49,9 @@ namespace {
 __device__ uint32_t g_err_bwd;
 
 constexpr int kThreads = 512;
-// Registers per thread at launch: 512 threads leave 128 each.  The launcher
-// checks that the compiled kernel uses exactly this many, because the
+// Registers per thread at launch: 512 threads leave 128 each.  The build
+// checks that the compiled d = 128 kernels use exactly this many, and the
+// launcher checks it again (FA_ERR_KERNEL_CONFIG otherwise), because the
 // setmaxnreg split below must add up to the launch allocation.
 constexpr int kRegLaunch = 128;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -692,7 +693,8 @@ fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
     // The setmaxnreg shares assume the launch allocation; with any other
     // count the dQ warpgroup's increase could never be granted.
     cudaFuncAttributes fattr{};
-    if (cudaFuncGetAttributes(&fattr, kern) != cudaSuccess || fattr.numRegs != kRegLaunch) return FA_ERR_LAUNCH;
+    if (cudaFuncGetAttributes(&fattr, kern) != cudaSuccess) return FA_ERR_LAUNCH;
+    if (fattr.numRegs != kRegLaunch) return FA_ERR_KERNEL_CONFIG;
   }
   const int n_blk = (a.N + 127) / 128;
   // Heads per group: Q, dO (bf16) and the dQ accumulator (fp32) of a group

@@ -393,7 +393,7 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // exp2_minimax.py beside this file); 2^n enters by an integer add into the
 // exponent field.  x is clamped to -126 first so the result stays a normal
 // number (2^-126 in place of smaller values).  Maximum relative error:
-// 1.7e-3 for DEG = 2, 7.5e-5 for DEG = 3.
+// 1.73e-3 for DEG = 2, 7.5e-5 for DEG = 3 (x in [-125.5, 127]).
 template <int DEG>
 __device__ __forceinline__ float2 exp2_poly2(float2 x) {
   static_assert(DEG == 2 || DEG == 3, "degree");

@@ -43,6 +43,8 @@
 // product is bound by shared-memory bandwidth rather than by the tensor core.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "fa_common.cuh"
 #include "fa_host.h"
 
@@ -178,6 +180,31 @@ __device__ __forceinline__ float exp2_pack_row(const float (&s)[kBN], float c, f
   return (part0.x + part0.y) + (part1.x + part1.y);
 }
 
+// Block index -> (query head, query block).  Query heads are taken in groups
+// whose keys and values stay in L2 together while every query block of the
+// group streams them; within a group, under a causal mask, the query blocks
+// that see the most keys (the last) come first.  A partial group (the
+// remainder of BH / group) goes first, so that the launch ends on the light
+// blocks of a full group.
+__device__ __forceinline__ void fwd_item(int item, int BH, int n_qblk, int group, int causal, int& bh, int& qb) {
+  const int rem = BH % group;
+  int g_heads, base_item, base_head;
+  if (item < rem * n_qblk) {
+    g_heads = rem;
+    base_item = 0;
+    base_head = 0;
+  } else {
+    const int g = (item - rem * n_qblk) / (group * n_qblk);
+    g_heads = group;
+    base_item = rem * n_qblk + g * group * n_qblk;
+    base_head = rem + g * group;
+  }
+  const int r = item - base_item;
+  const int step = r / g_heads;
+  qb = causal ? n_qblk - 1 - step : step;
+  bh = base_head + (r - step * g_heads);
+}
+
 // BS: block-quantised e4m3 inputs (one scale per 128 query rows and per 64
 // keys, of Q and of K and V), FP8 only.  WIN: causal sliding window.
 template <int D, bool FP8, bool BS, bool WIN>
@@ -186,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
                   float* __restrict__ out_lse, const float* __restrict__ descale_q,
                   const float* __restrict__ descale_k, const float* __restrict__ descale_v, int BH, int N,
-                  int causal, float scale_log2, int H, int qgroup, int window) {
+                  int causal, float scale_log2, int H, int qgroup, int window, int head_group) {
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmem sh;
@@ -199,12 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*reinterpret_cast<volatile uint32_t*>(&g_err_fwd) & FA_DEVERR_TIMEOUT) return;
   const int warp = warp_id();
   const int n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
-  // Longest rows first: under a causal mask the last query blocks of every
-  // head see the most keys, so they take the lowest block indices and are
-  // dispatched first.
-  const int item = static_cast<int>(blockIdx.x);
-  const int qb = causal ? (n_qblk - 1 - item / BH) : item / BH;
-  const int bh = item % BH;                       // query head
+  // Longest rows first within each L2-sized group of heads: under a causal
+  // mask the last query blocks of a head see the most keys, so they take the
+  // lowest block indices of their group and are dispatched first.
+  int bh, qb;  // query head, query block
+  fwd_item(static_cast<int>(blockIdx.x), BH, n_qblk, head_group, causal, bh, qb);
   // K/V head of this query head (grouped-query attention: qgroup consecutive
   // query heads share one; qgroup = 1 otherwise)
   const int bh_kv = (bh / H) * (H / qgroup) + (bh % H) / qgroup;
@@ -711,9 +737,16 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
     return FA_ERR_LAUNCH;
   dim3 grid(static_cast<unsigned>(((a.N + 2 * kBM - 1) / (2 * kBM)) * BH));
   const float scale_log2 = a.scale * 1.4426950408889634f;
+  // Query heads per group: the keys and values their blocks stream should
+  // stay within about 32 MB of the L2 (query heads of one key/value head
+  // share it).
+  const int qgroup = a.H / a.Hkv;
+  const long long kv_bytes_per_qhead = 2ll * a.N * D * C::kElemBytes / qgroup;
+  int group = static_cast<int>(std::max<long long>(1, (32ll << 20) / std::max<long long>(1, kv_bytes_per_qhead)));
+  group = std::min(group, BH);
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a.lse, a.descale_q,
                                                    a.descale_k, a.descale_v, BH, a.N, a.causal, scale_log2, a.H,
-                                                   a.H / a.Hkv, a.window);
+                                                   qgroup, a.window, group);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

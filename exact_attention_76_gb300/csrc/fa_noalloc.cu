@@ -21,7 +21,12 @@
 //    threads without ordering) race on the array.  Order them on one stream.
 //  * The first call on a device resolves the array's device address with
 //    cudaGetSymbolAddress, with that device current; make that first call
-//    before any stream capture.
+//    before any stream capture.  The address is kept together with the
+//    driver context it belongs to: after cudaDeviceReset (or under another
+//    context on the same device) the library's module is loaded afresh, so
+//    a call made under a context other than the recorded one looks the
+//    address up again instead of reusing a stale one.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -36,23 +41,71 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 
-// Device address of g_noalloc_scratch on the current device (set up once per
-// device).  In host code the array's name is only a host-side handle, never a
-// device address, so kernels receive this pointer instead.
+// cuCtxGetCurrent through the runtime's driver entry point (the library links
+// the static runtime and not libcuda directly), resolved once.
+CtxGetCurrentFn resolve_ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+std::mutex g_scratch_mu;
+struct ScratchAddr {
+  CUcontext ctx;
+  void* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+// The kernels of this library exist for sm_103 only: on any other device the
+// symbol lookup below would fail for want of a code image.
+fa_status check_current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return FA_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess)
+    return FA_ERR_UNSUPPORTED;
+  if (major != 10 || minor != 3) return FA_ERR_UNSUPPORTED;
+  if (*dev < 0 || *dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// Device address of g_noalloc_scratch for the current device and context
+// (looked up once per device and context).  In host code the array's name is
+// only a host-side handle, never a device address, so kernels receive this
+// pointer instead.
 fa_status scratch_for_current_device(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_UNSUPPORTED;
-  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  fa_status st = check_current_device(&dev);
+  if (st != FA_OK) return st;
+  CtxGetCurrentFn get_ctx = resolve_ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (get_ctx == nullptr || get_ctx(&ctx) != CUDA_SUCCESS) return FA_ERR_LAUNCH;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  ScratchAddr& e = g_scratch[dev];
+  if (e.ptr == nullptr || e.ctx != ctx || ctx == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FA_ERR_LAUNCH;
-    g_scratch_ptr[dev] = p;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // clear the failed lookup's error so that no later call reports it
+      e.ptr = nullptr;
+      return FA_ERR_LAUNCH;
+    }
+    // The runtime makes the primary context current during the lookup when
+    // none was: record the context the address now belongs to.
+    CUcontext now = nullptr;
+    if (get_ctx(&now) != CUDA_SUCCESS) return FA_ERR_LAUNCH;
+    e.ctx = now;
+    e.ptr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = e.ptr;
   return FA_OK;
 }
 

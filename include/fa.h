@@ -50,7 +50,11 @@ typedef enum {
   FA_ERR_ALIGNMENT = 3,   /* a tensor pointer not 16-byte aligned                */
   FA_ERR_LAUNCH = 4,      /* a kernel launch or tensor-map encoding failed       */
   FA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (fa_device_error)   */
-  FA_ERR_WORKSPACE = 6    /* workspace missing or smaller than required          */
+  FA_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required          */
+  FA_ERR_KERNEL_CONFIG = 7 /* the compiled kernel does not match the launch plan:
+                              its register count differs from the one its
+                              per-warpgroup register split assumes (a toolchain
+                              change); nothing was launched                      */
 } fa_status;
 
 /*
@@ -290,10 +294,28 @@ fa_status fa_device_error(void* stream);
  * results per clock per SM (two CTAs of 512 threads per SM, each thread 8
  * independent ex2 -> FMA chains).  The softmax of every kernel here costs one
  * exp2 per score, so this rate bounds it ("FLASH-ATTN", FlashAttention-3:
- * the exponential unit is far slower than the tensor cores).  Allocates and
- * frees its scratch on `stream` and synchronises it.
+ * the exponential unit is far slower than the tensor cores).
+ *   scratch : caller-owned DEVICE buffer of at least
+ *             fa_measure_ex2_rate_scratch_size() bytes (that size depends on
+ *             the current device's SM count), 16-byte aligned; overwritten.
+ * Synchronises `stream` (it reads the cycle counts back to the host).
  */
-fa_status fa_measure_ex2_rate(float* ex2_per_clock_per_sm, void* stream);
+size_t fa_measure_ex2_rate_scratch_size(void);
+fa_status fa_measure_ex2_rate(float* ex2_per_clock_per_sm, void* scratch, size_t scratch_bytes, void* stream);
+
+/*
+ * Test hook for the FMA-pipe exponential ("software exp2", named by the
+ * FlashAttention-4 summary in "FlashAttention 源码级深度解析" as a Blackwell
+ * lever): y[i] = 2^x[i] computed by the library's own polynomial (Cody-Waite
+ * split x = n + f, |f| <= 1/2, a minimax polynomial of `degree` 2 or 3 for
+ * 2^f, 2^n added into the exponent field; x below -126 is taken as -126), the
+ * same device function the forward kernel can use for part of its
+ * exponentials.  Maximum relative error 1.73e-3 at degree 2, 7.5e-5 at degree
+ * 3, for x in [-125.5, 127]; below that the result stands in for zero (it is
+ * at most 2^-125).
+ *   x, y : DEVICE fp32 arrays of n elements (n >= 1), 16-byte aligned.
+ */
+fa_status fa_debug_exp2_poly(const float* x, float* y, long long n, int degree, void* stream);
 
 /*
  * Test hook for the timeout path: launches one CTA whose thread waits on an

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = lib.fa_status_string(code).decode()
         assert s.startswith(_lib.STATUS_NAMES[code])
 
@@ -95,6 +95,16 @@ def test_fp8_argument_errors_before_any_launch(lib):
     assert lib.fa_fwd_fp8(p, p, p + 1, p, p, p, p, p, 1, 1, 128, 128, 0, 0.1, None) == 3
 
 
+def test_measurement_and_exp2_hooks_reject_bad_arguments(lib):
+    p = ALIGNED
+    assert lib.fa_measure_ex2_rate(None, p, 1 << 20, None) == 1
+    assert lib.fa_measure_ex2_rate(p, None, 1 << 20, None) == 1
+    assert lib.fa_measure_ex2_rate(p, p + 4, 1 << 20, None) == 3
+    assert lib.fa_debug_exp2_poly(p, p, 0, 3, None) == 1
+    assert lib.fa_debug_exp2_poly(p, p, 16, 4, None) == 1
+    assert lib.fa_debug_exp2_poly(None, p, 16, 3, None) == 1
+
+
 def test_debug_timeout_hook_rejects_bad_limit(lib):
     assert lib.fa_debug_wait_timeout(0, None) == 1
     assert lib.fa_debug_wait_timeout(2_000_000, None) == 1
@@ -107,3 +117,17 @@ def test_product_has_no_oracle_import():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_build_register_check_reads_the_ptxas_report():
+    log = ("ptxas info    : Compiling entry function '_ZN2fa4anon18fa_bwd_main_kernelILi128ELb0EEEv' for 'sm_103a'\n"
+           "ptxas info    : Function properties for _ZN2fa4anon18fa_bwd_main_kernelILi128ELb0EEEv\n"
+           "    8 bytes stack frame, 0 bytes spill stores, 0 bytes spill loads\n"
+           "ptxas info    : Used {} registers, used 2 barriers\n"
+           "ptxas info    : Compiling entry function '_ZN2fa4anon18fa_bwd_main_kernelILi64ELb0EEEv' for 'sm_103a'\n"
+           "ptxas info    : Used 96 registers, used 2 barriers\n")
+    build.check_registers(log.format(128), "fa_bwd_main_kernelILi128E", 128, "fa_bwd.cu")
+    with pytest.raises(RuntimeError, match="uses 120 registers"):
+        build.check_registers(log.format(120), "fa_bwd_main_kernelILi128E", 128, "fa_bwd.cu")
+    with pytest.raises(RuntimeError, match="no register report"):
+        build.check_registers("", "fa_bwd_main_kernelILi128E", 128, "fa_bwd.cu")

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from exact_attention_76_gb300 import api, build, inputs
-from tests.gpu_util import FP8_O_REL_FRO, GRAD_REL_FRO, L_MAX_ABS, O_MAX_ABS, f64, max_abs, rel_fro
+from tests.gpu_util import FP8_O_REL_FRO, GRAD_REL_FRO, L_MAX_ABS, O_MAX_ABS, f64, max_abs, o_report, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -20,7 +20,7 @@ def built():
     assert api.fa_device_error() == 0
 
 
-def _fwd_bwd_sampled(B, H, N, d, causal, seed, heads):
+def _fwd_bwd_sampled(B, H, N, d, causal, seed, heads, label):
     scale = 1.0 / math.sqrt(d)
     q, k, v, do = inputs.draw_bf16(B, H, N, d, seed)
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
@@ -28,27 +28,30 @@ def _fwd_bwd_sampled(B, H, N, d, causal, seed, heads):
     dq, dk, dv = api.fa_bwd(qd, kd, vd, o, lse, dod, causal, scale)
     torch.cuda.synchronize()
     o_ref, l_ref = oracle.forward(q, k, v, causal, scale, heads=heads)
+    absv_ref, _ = oracle.forward(q, k, v.abs(), causal, scale, heads=heads)
     g_ref = oracle.backward(q, k, v, do, causal, scale, heads=heads)
     eo, el = max_abs(f64(o), o_ref), max_abs(f64(lse), l_ref)
     eg = [rel_fro(f64(g), r) for g, r in zip((dq, dk, dv), g_ref)]
     assert eo <= O_MAX_ABS, f"O max-abs {eo:.3e}"
     assert el <= L_MAX_ABS, f"L max-abs {el:.3e}"
+    o_report(f64(o), o_ref, absv_ref, N, label)
     for name, e in zip(("dQ", "dK", "dV"), eg):
         assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e}"
 
 
 def test_long_causal_workload_sampled_heads():
     w = inputs.LONG_CAUSAL
-    _fwd_bwd_sampled(w.B, w.H, w.N, w.d, w.causal, w.seed, heads=[(0, 0), (1, 15)])
+    _fwd_bwd_sampled(w.B, w.H, w.N, w.d, w.causal, w.seed, heads=[(0, 0), (1, 15)], label=w.name)
 
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N", [512, 2048, 8192, 16384])
+@pytest.mark.parametrize("N", [512, 1024, 2048, 4096, 8192, 16384])
 def test_fixed_token_sweep_sampled_head(N, causal, d):
+    # every length of the fixed-16384-token sweep, in its own launch shape
     ws = {w.N: w for w in inputs.sweep_workloads(causal, d)}
     w = ws[N]
-    _fwd_bwd_sampled(w.B, w.H, w.N, w.d, causal, w.seed, heads=[(w.B - 1, w.H - 1)])
+    _fwd_bwd_sampled(w.B, w.H, w.N, w.d, causal, w.seed, heads=[(w.B - 1, w.H - 1)], label=w.name)
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -5,9 +5,11 @@ the library instead of a caller workspace.
 
 Checked here through the C ABI: two calls in a row (different inputs, so the
 second would expose stale scratch) each match what fa_bwd with a caller
-workspace produces, within the gradient tolerance every backward test uses;
-a problem needing more than the array returns FA_ERR_WORKSPACE.  This file
-is collected last on purpose."""
+workspace produces, within the gradient tolerance every backward test uses,
+for a small causal d = 128 case, a non-causal d = 64 case and a case whose
+workspace is just under the array's 32 MiB (so the far end of the array is
+used); a problem needing more than the array returns FA_ERR_WORKSPACE.  This
+file is collected last on purpose."""
 import ctypes
 import math
 
@@ -26,10 +28,15 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def test_noalloc_backward_matches_workspace_backward_twice():
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (2, 3, 333, 128, True),
+    (1, 5, 700, 64, False),
+    (1, 4, 16000, 128, True),   # workspace 33.02 MB, just under the 33.55 MB array
+])
+def test_noalloc_backward_matches_workspace_backward_twice(B, H, N, d, causal):
     build.build()
     lib = _lib.load()
-    B, H, N, d, causal = 2, 3, 333, 128, True
+    assert api.fa_bwd_workspace_size(B, H, N, d) <= 32 << 20
     scale = 1.0 / math.sqrt(d)
     stream = torch.cuda.current_stream()
     for call, seed in enumerate((41, 42)):
