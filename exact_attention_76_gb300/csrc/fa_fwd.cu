@@ -11,7 +11,7 @@
 // How it maps to the SM (one CTA = 256 query rows of one (batch, head)):
 //  * warps 0-3 and 4-7: two softmax warpgroups, one per 128-row query tile;
 //    thread r of a warpgroup owns row r (TMEM lane r);
-//  * warp 8: TMA producer -- the two Q tiles once, then K_j and V_j (64 keys
+//  * warp 8: TMA producer -- the two Q tiles once, then K_j and V_j (128 keys
 //    each) into a ring of shared-memory slots guarded by full/empty mbarriers
 //    (the producer/consumer split of "FLASH-ATTN", FlashAttention-3 >
 //    Producer-Consumer asynchrony);
@@ -19,28 +19,32 @@
 //    S_t = Q_t K_j^T (both operands in shared memory) and O_t += P_t V_j with
 //    P_t read from TMEM.
 //
-// Each query tile has its own S, P and O columns in TMEM, so the next S_t can
-// be computed as soon as the softmax warpgroup has copied the current S_t into
-// registers, while it is still exponentiating; the products of the other tile
-// fill the tensor pipe meanwhile (the two-stage and ping-pong overlaps of
-// "FLASH-ATTN", FlashAttention-3).  Per key block j and tile t the single MMA
-// thread issues S_t(j+1) (after the warpgroup released S_t(j)) and then
-// PV_t(j) (after it wrote P_t(j)).
+// Per query tile t the tensor core computes S_t(j) with N = 128 keys; the
+// softmax warpgroup reads S_t(j) into registers and writes P_t(j) into the
+// first columns of S_t's own TMEM space; the MMA thread then issues
+// O_t += P_t(j) V_j and, at once, S_t(j+1) into the same columns.  The
+// tcgen05.mma operations of one thread execute in issue order, so S_t(j+1)
+// overwrites P_t(j) only after PV_t(j) has read it, with no wait in between.
+// The two tiles alternate on the tensor core (PV_0, S_0, PV_1, S_1, ...), so
+// one warpgroup's softmax overlaps the other tile's two products (the
+// ping-pong of two consumer warpgroups, "FLASH-ATTN", FlashAttention-3).  A
+// completed S_t(j) also means that PV_t(j-1), issued before it, is complete,
+// so the warpgroup may rescale O_t right after reading S_t(j).
 //
 // Softmax works in the log2 domain: x = S * (scale * log2 e) with one FMA, then
 // ex2.  The reference maximum m_used is raised only when a block's maximum
 // exceeds it by more than TAU (8 for bf16, i.e. values up to 2^8 before a
 // rescale; 4 for e4m3, whose P * 2^4 must stay below 448); raising it
-// rescales l and the warpgroup's own O row in TMEM once the previous PV has
-// completed.  Any TAU gives the same exact result.  Each exponential is packed
-// into its P word as soon as it is computed; the e4m3 factor 2^4 is folded
-// into the exponent.
+// rescales l and the warpgroup's own O row in TMEM.  Any TAU gives the same
+// exact result.  Each exponential is packed into its P word as soon as it is
+// computed; the e4m3 factor 2^4 is folded into the exponent.
 //
-// TMEM columns: S_0 [0,64), S_1 [64,128), P_0 from 128, P_1 from 160,
-// Q_0 from 192 (Q_1 from 224 when a Q row is 128 bytes), O_0 [256,256+D),
-// O_1 [256+D,256+2D).  A tile whose Q sits in TMEM reads only K from shared
-// memory for S = Q K^T; with both operands in shared memory an M=128, N=64
-// product is bound by shared-memory bandwidth rather than by the tensor core.
+// TMEM columns: S_0 [0,128), S_1 [128,256) (P_t in the first 64 columns of
+// S_t for bf16, the first 32 for e4m3), O_0 [256,256+D), O_1 [256+D,256+2D).
+// Q stays in shared memory: an M = 128, N = 128 product with both operands in
+// shared memory uses the full shared-memory operand bandwidth, not more
+// (measured: 64 cycles per K = 16 step, the tensor core's own rate); with
+// 64-key blocks the N = 64 products of S took 48-50 cycles for half the work.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -56,79 +60,7 @@ __device__ uint32_t g_err_fwd;
 
 constexpr int kThreads = 320;
 constexpr int kBM = 128;  // query rows per tile (one TMEM lane each)
-constexpr int kBN = 64;   // keys per key/value block
-
-template <int D, bool FP8>
-struct FwdCfg {
-  static constexpr int kElemBytes = FP8 ? 1 : 2;
-  static constexpr int kRowBytes = D * kElemBytes;       // bytes of one row of Q/K/V
-  static constexpr int kColBlocks = kRowBytes / 128;     // 128-byte column blocks
-  static constexpr int kBoxCols = 128 / kElemBytes;      // elements per TMA box row
-  static constexpr int kQBlockBytes = kBM * 128;         // one column block of a Q tile
-  static constexpr int kQTileBytes = kBM * kRowBytes;
-  static constexpr int kOColBlocks = D * 2 / 128;                // 128-byte column blocks of a bf16 O row
-  static constexpr int kOStageBlocks = kQTileBytes / kQBlockBytes;  // O blocks that fit in a Q tile
-  static constexpr int kKVBlockBytes = kBN * 128;        // one column block of a K/V tile
-  static constexpr int kKVTileBytes = kBN * kRowBytes;
-  static constexpr int kSlots = 131072 / kKVTileBytes;   // 128 KB ring
-  static constexpr int kSmemBytes = 2 * kQTileBytes + kSlots * kKVTileBytes + 1024;
-  static constexpr int kKPerMma = FP8 ? 32 : 16;         // K extent of one MMA
-  static constexpr int kQKSteps = kRowBytes / 32;        // MMAs for S = Q K^T
-  static constexpr int kPVSteps = kBN / kKPerMma;        // MMAs for O += P V
-  // e4m3 P is stored as P * 2^4 and the largest e4m3 value is 448, so P may
-  // reach 2^4 (P * 2^4 <= 256) before the reference max must move.  The
-  // factor trades headroom against the range of small P (normal down to
-  // 2^-10): measured on the outlier inputs, 2^8 with TAU 0.75 rescaled O so
-  // often that the forward ran 7 % slower for 0.08 points less error.
-  static constexpr float kTauLog2 = FP8 ? 4.0f : 8.0f;
-  // P goes to the e4m3 operand as P * 2^4: the factor enters the exponent
-  // (m - 4), so the row sum l and O~ both carry it and it cancels in O~ / l.
-  static constexpr float kPShiftLog2 = FP8 ? -4.0f : 0.0f;
-  static constexpr int kPWords = FP8 ? kBN / 4 : kBN / 2;  // 32-bit words of one P row
-  // Exponentials on the FMA pipes ("software exp2"): groups of four (of
-  // kBN / 4) per row and block taken by the polynomial, and its degree (bf16 P
-  // keeps 8 significant bits, e4m3 P 4).  Measured on GB300 it only costs
-  // time: with 2, 4 and 6 of 16 groups the d = 64 forward ran 7, 11 and 18 %
-  // slower and the d = 128 one 0-2 % slower, so no group uses it.
-  static constexpr int kEmuGroups = 0;
-  static constexpr int kPolyDeg = FP8 ? 2 : 3;
-  // Speculative exponentials (below) shorten the softmax when it bounds the
-  // key-block period (bf16 at d = 64: +6 to +8 % measured); at d = 128 the
-  // period is set by the products and the variant measured 2-3 % slower.
-  static constexpr bool kSpecExp = !FP8 && D == 64;
-  static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(128, kBN, false, false) : idesc_bf16(128, kBN, false, false);
-  static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
-  static constexpr uint32_t kTmS = 0;     // + t * kBN
-  static constexpr uint32_t kTmP = 128;   // + t * 32
-  static constexpr uint32_t kTmO = 256;   // + t * D
-  // Q kept in TMEM (A operand of S read from TMEM instead of shared memory):
-  // one row of Q needs kRowBytes / 4 columns; tile 0 always fits in the free
-  // columns [192, 256), tile 1 too when a row is at most 128 bytes.
-  static constexpr int kQCols = kRowBytes / 4;
-  static constexpr uint32_t kTmQ = 192;   // + t * kQCols
-  static constexpr bool kQTm1 = kQCols <= 32;
-  static_assert(D == 64 || D == 128, "head dim");
-  static_assert(kColBlocks >= 1, "row must fill a 128-byte swizzle row");
-  static_assert(kSlots <= 16, "barrier arrays");
-  static_assert(kTmQ + (kQTm1 ? 2 : 1) * kQCols <= kTmO, "TMEM columns for Q");
-  static_assert(kOStageBlocks >= 1 && kOColBlocks % kOStageBlocks == 0, "O staging");
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
-};
-
-struct FwdSmem {
-  uint64_t q_full;
-  uint64_t q_tm[2];
-  uint64_t kv_full[16];
-  uint64_t kv_empty[16];
-  uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full[2];
-  uint64_t o_done[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  float vmax_part[2][4];
-  CtaAbort abort;
-};
+constexpr int kHalf = 64;  // keys per half block (one exp2_pack_row call)
 
 __device__ __forceinline__ void issue_mma(bool fp8, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if (fp8) mma_f8_ss(d, a, b, idesc, acc);
@@ -140,24 +72,24 @@ __device__ __forceinline__ void issue_mma_ts(bool fp8, uint32_t d, uint32_t a, u
   else mma_bf16_ts(d, a, b, idesc, acc);
 }
 
-// P for one row of a key block: p_i = 2^(s_i * c - m), packed into the words
+// P for 64 keys of one row: p_i = 2^(s_i * c - m), packed into the words
 // written to TMEM (bf16 pairs, or four e4m3); returns the sum of the p_i.  The
-// scores s are left unchanged.  EMU of the kBN / 4 groups of four use the
+// scores s are left unchanged.  EMU of the 16 groups of four use the
 // polynomial exp2 (spread evenly), the rest ex2.approx.  With PMUL the e4m3
 // words hold p_i * pmul (the block-quantised V's relative scale).
 template <bool FP8, int EMU, int DEG, bool PMUL = false>
-__device__ __forceinline__ float exp2_pack_row(const float (&s)[kBN], float c, float m,
-                                               uint32_t (&pw)[FP8 ? kBN / 4 : kBN / 2], float pmul = 1.0f) {
+__device__ __forceinline__ float exp2_pack_row(const float (&s)[kHalf], float c, float m,
+                                               uint32_t (&pw)[FP8 ? kHalf / 4 : kHalf / 2], float pmul = 1.0f) {
   const float2 c2 = make_float2(c, c);
   const float2 nm2 = make_float2(-m, -m);
   float2 part0 = make_float2(0.f, 0.f), part1 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < kBN; i += 4) {
+  for (int i = 0; i < kHalf; i += 4) {
     const int g = i / 4;
     const float2 x0 = __ffma2_rn(make_float2(s[i], s[i + 1]), c2, nm2);
     const float2 x1 = __ffma2_rn(make_float2(s[i + 2], s[i + 3]), c2, nm2);
     float2 y0, y1;
-    if (((g + 1) * EMU) / (kBN / 4) != (g * EMU) / (kBN / 4)) {
+    if (((g + 1) * EMU) / (kHalf / 4) != (g * EMU) / (kHalf / 4)) {
       y0 = exp2_poly2<DEG>(x0);
       y1 = exp2_poly2<DEG>(x1);
     } else {
@@ -205,42 +137,74 @@ __device__ __forceinline__ void fwd_item(int item, int BH, int n_qblk, int group
   bh = base_head + (r - step * g_heads);
 }
 
-// BS: block-quantised e4m3 inputs (one scale per 128 query rows and per 64
-// keys, of Q and of K and V), FP8 only.  WIN: causal sliding window.
+constexpr int kBN = 128;  // keys per key/value block
+
+template <int D, bool FP8>
+struct FwdCfg {
+  static constexpr int kElemBytes = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElemBytes;
+  static constexpr int kColBlocks = kRowBytes / 128;
+  static constexpr int kBoxCols = 128 / kElemBytes;
+  static constexpr int kBlockBytes = 128 * 128;          // one 128-row x 128-byte column block
+  static constexpr int kTileBytes = 128 * kRowBytes;     // a Q tile or a K / V block
+  static constexpr int kOColBlocks = D * 2 / 128;
+  static constexpr int kOStageBlocks = kTileBytes / kBlockBytes;
+  static constexpr int kSlotsFit = (232448 - 1024 - 1024 - 2 * kTileBytes) / kTileBytes;
+  static constexpr int kSlots = kSlotsFit > 16 ? 16 : kSlotsFit;
+  static constexpr int kSmemBytes = 2 * kTileBytes + kSlots * kTileBytes + 1024;
+  static constexpr int kKPerMma = FP8 ? 32 : 16;
+  static constexpr int kQKSteps = kRowBytes / 32;
+  static constexpr int kPVSteps = kBN / kKPerMma;
+  static constexpr float kTauLog2 = FP8 ? 4.0f : 8.0f;
+  static constexpr float kPShiftLog2 = FP8 ? -4.0f : 0.0f;
+  static constexpr int kPWordsHalf = FP8 ? 16 : 32;      // TMEM words of P per 64 keys
+  static constexpr uint32_t kIdescS = FP8 ? idesc_e4m3(128, kBN, false, false) : idesc_bf16(128, kBN, false, false);
+  static constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
+  static constexpr uint32_t kTmS = 0;     // + t * 128
+  static constexpr uint32_t kTmO = 256;   // + t * D
+  static_assert(D == 64 || D == 128, "head dim");
+  static_assert(kSlots >= 4, "K/V ring depth");
+  static_assert(kOStageBlocks >= 1 && kOColBlocks % kOStageBlocks == 0, "O staging");
+  static_assert(kSmemBytes <= 232448 - 1024, "shared memory budget");
+};
+
+struct FwdSmem {
+  uint64_t q_full;
+  uint64_t kv_full[16];
+  uint64_t kv_empty[16];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  float vmax_part[2][4];
+  CtaAbort abort;
+};
+
 template <int D, bool FP8, bool BS, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
-                  float* __restrict__ out_lse, const float* __restrict__ descale_q,
-                  const float* __restrict__ descale_k, const float* __restrict__ descale_v, int BH, int N,
-                  int causal, float scale_log2, int H, int qgroup, int window, int head_group) {
+                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_o,
+                   float* __restrict__ out_lse, const float* __restrict__ descale_q,
+                   const float* __restrict__ descale_k, const float* __restrict__ descale_v, int BH, int N,
+                   int causal, float scale_log2, int H, int qgroup, int window, int head_group) {
   using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ FwdSmem sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_q = smem;                        // two Q tiles
-  uint8_t* s_kv = smem + 2 * C::kQTileBytes;  // ring of K/V slots
+  uint8_t* s_q = smem;                       // two Q tiles
+  uint8_t* s_kv = smem + 2 * C::kTileBytes;  // ring of K/V slots
 
-  // A wait of an earlier CTA ran out: the launch is already failed, stop here
-  // (the word stays set until fa_device_error reads and clears it).
   if (*reinterpret_cast<volatile uint32_t*>(&g_err_fwd) & FA_DEVERR_TIMEOUT) return;
   const int warp = warp_id();
   const int n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
-  // Longest rows first within each L2-sized group of heads: under a causal
-  // mask the last query blocks of a head see the most keys, so they take the
-  // lowest block indices of their group and are dispatched first.
-  int bh, qb;  // query head, query block
+  int bh, qb;
   fwd_item(static_cast<int>(blockIdx.x), BH, n_qblk, head_group, causal, bh, qb);
-  // K/V head of this query head (grouped-query attention: qgroup consecutive
-  // query heads share one; qgroup = 1 otherwise)
   const int bh_kv = (bh / H) * (H / qgroup) + (bh % H) / qgroup;
   const int q0 = qb * 2 * kBM;
   const int n_kv_all = (N + kBN - 1) / kBN;
-  // Tile t visits key blocks j_lo[t] .. n_t[t] - 1 (len[t] of them): all blocks
-  // up to the causal limit, and with a sliding window of `window` keys
-  // (window > 0, causal) none that lies entirely before the window of the
-  // tile's first row.  Tile 0's range starts first; together the two ranges
-  // cover j_begin .. n_max - 1 without a gap.
+  // Tile t visits key blocks j_lo[t] .. n_t[t] - 1 (len[t] of them); tile 0's
+  // range starts first and the two ranges cover j_begin .. n_max - 1.
   int n_t[2], j_lo[2], len[2];
   for (int t = 0; t < 2; ++t) {
     const int row0 = q0 + t * kBM;
@@ -259,15 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     sh.abort.flag = 0;
     mbar_init(&sh.q_full, 1);
-    mbar_init(&sh.q_tm[0], kBM);
-    mbar_init(&sh.q_tm[1], kBM);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(&sh.kv_full[s], 1);
       mbar_init(&sh.kv_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sh.s_full[t], 1);
-      mbar_init(&sh.s_free[t], kBM);
       mbar_init(&sh.p_full[t], kBM);
       mbar_init(&sh.o_done[t], 1);
     }
@@ -286,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(&sh.q_full, 2 * C::kQTileBytes);
+      mbar_arrive_expect_tx(&sh.q_full, 2 * C::kTileBytes);
       for (int t = 0; t < 2; ++t)
         for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d(s_q + t * C::kQTileBytes + cb * C::kQBlockBytes, &map_q, cb * C::kBoxCols, q0 + t * kBM, bh,
+          tma_load_3d(s_q + t * C::kTileBytes + cb * C::kBlockBytes, &map_q, cb * C::kBoxCols, q0 + t * kBM, bh,
                       &sh.q_full);
       int issued = 0;
       for (int j = j_begin; j < n_max && !sh.abort.flag; ++j) {
@@ -297,16 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int slot = issued % C::kSlots;
           const int round = issued / C::kSlots;
           if (round > 0 && !mbar_wait<true>(&sh.kv_empty[slot], (round - 1) & 1, &sh.abort, &g_err_fwd)) break;
-          mbar_arrive_expect_tx(&sh.kv_full[slot], C::kKVTileBytes);
+          mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
           const CUtensorMap* m = kv == 0 ? &map_k : &map_v;
           for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(s_kv + slot * C::kKVTileBytes + cb * C::kKVBlockBytes, m, cb * C::kBoxCols, j * kBN, bh_kv,
+            tma_load_3d(s_kv + slot * C::kTileBytes + cb * C::kBlockBytes, m, cb * C::kBoxCols, j * kBN, bh_kv,
                         &sh.kv_full[slot]);
           ++issued;
         }
       }
       if (sh.abort.flag) {
-        // Let every copy still in flight land before the CTA's memory goes away.
         mbar_wait_drain(&sh.q_full, 0, &g_err_fwd);
         for (int s = 0; s < C::kSlots && s < issued; ++s) {
           const int last = s + ((issued - 1 - s) / C::kSlots) * C::kSlots;
@@ -318,33 +278,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one() && n_max > 0) {
-      // Base descriptors; every operand below is one of these advanced by a
-      // byte offset that is a compile-time constant after unrolling.
-      const uint64_t q_desc = sdesc_sw128(smem_u32(s_q), 16, 1024);                     // K-major Q tiles
-      const uint64_t k_desc = sdesc_sw128(smem_u32(s_kv), 16, 1024);                    // K-major K slots
-      const uint64_t v_desc = sdesc_sw128(smem_u32(s_kv), C::kKVBlockBytes, 1024);      // MN-major V slots
+      const uint64_t q_desc = sdesc_sw128(smem_u32(s_q), 16, 1024);                  // K-major Q tiles
+      const uint64_t k_desc = sdesc_sw128(smem_u32(s_kv), 16, 1024);                 // K-major K slots
+      const uint64_t v_desc = sdesc_sw128(smem_u32(s_kv), C::kBlockBytes, 1024);     // MN-major V slots
       auto issue_s = [&](int t, int slot) {
-        const uint64_t b0 = sdesc_advance(k_desc, slot * C::kKVTileBytes);
-        if (t == 0 || C::kQTm1) {  // Q from TMEM: only K is read from shared memory
-          const uint32_t a_tm = tmem + C::kTmQ + t * C::kQCols;
+        const uint64_t a0 = sdesc_advance(q_desc, t * C::kTileBytes);
+        const uint64_t b0 = sdesc_advance(k_desc, slot * C::kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < C::kQKSteps; ++kk)
-            issue_mma_ts(FP8, tmem + C::kTmS + t * kBN, a_tm + kk * 8,
-                         sdesc_advance(b0, (kk >> 2) * C::kKVBlockBytes + (kk & 3) * 32), C::kIdescS, kk > 0);
-        } else {
-          const uint64_t a0 = sdesc_advance(q_desc, t * C::kQTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < C::kQKSteps; ++kk) {
-            const uint32_t in_row = (kk & 3) * 32;
-            issue_mma(FP8, tmem + C::kTmS + t * kBN, sdesc_advance(a0, (kk >> 2) * C::kQBlockBytes + in_row),
-                      sdesc_advance(b0, (kk >> 2) * C::kKVBlockBytes + in_row), C::kIdescS, kk > 0);
-          }
+        for (int kk = 0; kk < C::kQKSteps; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          issue_mma(FP8, tmem + C::kTmS + t * kBN, sdesc_advance(a0, off), sdesc_advance(b0, off), C::kIdescS,
+                    kk > 0);
         }
         tc_commit(&sh.s_full[t]);
       };
       auto issue_pv = [&](int t, int slot, bool acc) {
-        const uint64_t b0 = sdesc_advance(v_desc, slot * C::kKVTileBytes);
-        const uint32_t a_tm = tmem + C::kTmP + t * 32;
+        const uint64_t b0 = sdesc_advance(v_desc, slot * C::kTileBytes);
+        const uint32_t a_tm = tmem + C::kTmS + t * kBN;  // P over S_t
         const uint32_t d_tm = tmem + C::kTmO + t * D;
 #pragma unroll
         for (int kk = 0; kk < C::kPVSteps; ++kk)
@@ -355,153 +305,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_load = [&](int idx) {
         return mbar_wait<true>(&sh.kv_full[idx % C::kSlots], (idx / C::kSlots) & 1, &sh.abort, &g_err_fwd);
       };
-      if constexpr (!WIN) {
-        bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd) && wait_load(0);
-        if (ok) {
-          tc_fence_after();
-          // Tile 1 first: its Q may come from shared memory, while tile 0's Q is
-          // still being copied into TMEM by its warpgroup.
-          for (int t = 1; ok && t >= 0; --t) {
-            if (n_t[t] == 0) continue;
-            if (t == 0 || C::kQTm1) {
-              ok = mbar_wait<true>(&sh.q_tm[t], 0, &sh.abort, &g_err_fwd);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            issue_s(t, 0);
-          }
-          if (ok) tc_commit(&sh.kv_empty[0]);
-        }
-        for (int j = 0; ok && j < n_max; ++j) {
-          const int k_idx = 2 * j + 2;  // K_(j+1)
-          const int v_idx = 2 * j + 1;  // V_j
-          bool k_ready = false, v_ready = false;
-          for (int t = 0; ok && t < 2; ++t) {
-            // S_t(j+1): its columns are free once the warpgroup copied S_t(j) out.
-            if (j + 1 < n_t[t]) {
-              if (!k_ready) {
-                ok = wait_load(k_idx);
-                k_ready = true;
-              }
-              ok = ok && mbar_wait<true>(&sh.s_free[t], j & 1, &sh.abort, &g_err_fwd);
-              if (!ok) break;
-              tc_fence_after();
-              issue_s(t, k_idx % C::kSlots);
-            }
-            // PV_t(j) once the warpgroup wrote P_t(j).
-            if (j < n_t[t]) {
-              if (!v_ready) {
-                ok = wait_load(v_idx);
-                v_ready = true;
-              }
-              ok = ok && mbar_wait<true>(&sh.p_full[t], j & 1, &sh.abort, &g_err_fwd);
-              if (!ok) break;
-              tc_fence_after();
-              issue_pv(t, v_idx % C::kSlots, j > 0);
-            }
-          }
-          if (!ok) break;
-          if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
-          if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
-        }
-      } else {
-        // Load index of K_j is 2 (j - j_begin), of V_j one more (the producer's
-        // order).  Tile t's step u is key block j_lo[t] + u.
-        auto k_load = [&](int j) { return 2 * (j - j_begin); };
-        // The first S of a tile needs its Q in place: tiles whose Q sits in TMEM
-        // wait for their warpgroup's copy.
-        auto wait_q = [&](int t) {
-          if (t != 0 && !C::kQTm1) return true;
-          if (!mbar_wait<true>(&sh.q_tm[t], 0, &sh.abort, &g_err_fwd)) return false;
-          tc_fence_after();
-          return true;
-        };
-        bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd) && wait_load(k_load(j_begin));
-        if (ok) {
-          tc_fence_after();
-          // Tile 1 first: its Q may come from shared memory, while tile 0's Q is
-          // still being copied into TMEM by its warpgroup.
-  #pragma unroll
-          for (int t = 1; t >= 0; --t) {
-            if (!ok || len[t] <= 0 || j_lo[t] != j_begin) continue;
-            ok = wait_q(t);
-            if (ok) issue_s(t, k_load(j_begin) % C::kSlots);
-          }
-          if (ok) tc_commit(&sh.kv_empty[k_load(j_begin) % C::kSlots]);
-        }
-        for (int j = j_begin; ok && j < n_max; ++j) {
-          const int k_idx = k_load(j + 1);  // K_(j+1)
-          const int v_idx = k_load(j) + 1;  // V_j
-          bool k_ready = false, v_ready = false;
-  #pragma unroll
-          for (int t = 0; t < 2; ++t) {  // unrolled: the per-tile values stay in registers
-            if (!ok) break;
-            const int u = j - j_lo[t];
-            // S_t(u+1): its columns are free once the warpgroup copied S_t(u) out.
-            if (u + 1 >= 0 && u + 1 < len[t]) {
-              if (!k_ready) {
-                ok = wait_load(k_idx);
-                k_ready = true;
-              }
-              if (u >= 0) ok = ok && mbar_wait<true>(&sh.s_free[t], u & 1, &sh.abort, &g_err_fwd);
-              else ok = ok && wait_q(t);
-              if (!ok) break;
-              tc_fence_after();
-              issue_s(t, k_idx % C::kSlots);
-            }
-            // PV_t(u) once the warpgroup wrote P_t(u).
-            if (u >= 0 && u < len[t]) {
-              if (!v_ready) {
-                ok = wait_load(v_idx);
-                v_ready = true;
-              }
-              ok = ok && mbar_wait<true>(&sh.p_full[t], u & 1, &sh.abort, &g_err_fwd);
-              if (!ok) break;
-              tc_fence_after();
-              issue_pv(t, v_idx % C::kSlots, u > 0);
-            }
-          }
-          if (!ok) break;
-          if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
-          if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
-        }
+      // Load index of K_j is 2 (j - j_begin), of V_j one more.
+      auto k_load = [&](int j) { return 2 * (j - j_begin); };
+      bool ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd) && wait_load(k_load(j_begin));
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (len[t] > 0 && j_lo[t] == j_begin) issue_s(t, k_load(j_begin) % C::kSlots);
+        tc_commit(&sh.kv_empty[k_load(j_begin) % C::kSlots]);
       }
-      // Teardown: every MMA issued by this thread completes before TMEM is freed.
+      for (int j = j_begin; ok && j < n_max; ++j) {
+        const int k_idx = k_load(j + 1);  // K_(j+1)
+        const int v_idx = k_load(j) + 1;  // V_j
+        bool k_ready = false, v_ready = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok) break;
+          const int u = j - j_lo[t];
+          // PV_t(u) once the warpgroup wrote P_t(u) over S_t(u) ...
+          if (u >= 0 && u < len[t]) {
+            if (!v_ready) {
+              ok = wait_load(v_idx);
+              v_ready = true;
+            }
+            ok = ok && mbar_wait<true>(&sh.p_full[t], u & 1, &sh.abort, &g_err_fwd);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, v_idx % C::kSlots, u > 0);
+          }
+          // ... and right behind it S_t(u+1) into the same columns.
+          if (u + 1 >= 0 && u + 1 < len[t]) {
+            if (!k_ready) {
+              ok = wait_load(k_idx);
+              k_ready = true;
+              if (!ok) break;
+              tc_fence_after();
+            }
+            issue_s(t, k_idx % C::kSlots);
+          }
+        }
+        if (!ok) break;
+        if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
+        if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
+      }
       tc_commit(&sh.drain);
       mbar_wait_drain(&sh.drain, 0, &g_err_fwd);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;              // query tile of this warpgroup
-    const int r = threadIdx.x & 127;      // row within the tile == TMEM lane
+    const int t = warp >> 2;
+    const int r = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_base + C::kTmS + t * kBN;
-    const uint32_t p_col = tmem + lane_base + C::kTmP + t * 32;
     const uint32_t o_col = tmem + lane_base + C::kTmO + t * D;
     const int row_g = q0 + t * kBM + r;
-    const int jlo_t = t ? j_lo[1] : j_lo[0];  // first key block of this tile
-    const int nt = t ? len[1] : len[0];       // key blocks it visits
+    const int jlo_t = t ? j_lo[1] : j_lo[0];
+    const int nt = t ? len[1] : len[0];
+    const int n64 = (N + 63) / 64;  // 64-key scale blocks (block-quantised K and V)
     float c = scale_log2;
     float o_mult = 1.0f;
     if constexpr (FP8 && !BS) {
       c = scale_log2 * __ldg(descale_q) * __ldg(descale_k);
       o_mult = __ldg(descale_v);
     }
-    // Block scales ("FLASH-ATTN", FlashAttention-3 > Low-precision with FP8,
-    // block quantisation): S of query block t and key block j is scaled by
-    // delta_q(t) delta_k(j); V's block scale delta_v(j) goes into P's e4m3
-    // operand relative to the head's largest one, which O takes at the end.
-    float cq = 0.f, inv_vmax = 1.f, dk_cur = 0.f, dv_cur = 0.f;
+    float cq = 0.f, inv_vmax = 1.f;
     const float* dk_row = nullptr;
     const float* dv_row = nullptr;
     if constexpr (BS) {
-      dk_row = descale_k + static_cast<size_t>(bh_kv) * n_kv_all;
-      dv_row = descale_v + static_cast<size_t>(bh_kv) * n_kv_all;
+      dk_row = descale_k + static_cast<size_t>(bh_kv) * n64;
+      dv_row = descale_v + static_cast<size_t>(bh_kv) * n64;
       if (nt > 0) {  // uniform over the warpgroup
         cq = scale_log2 * __ldg(descale_q + static_cast<size_t>(bh) * ((N + kBM - 1) / kBM) + q0 / kBM + t);
         float vm = 0.f;
-        for (int jj = r; jj < n_kv_all; jj += kBM) vm = fmaxf(vm, __ldg(dv_row + jj));
+        for (int jj = r; jj < n64; jj += kBM) vm = fmaxf(vm, __ldg(dv_row + jj));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, off));
         if ((r & 31) == 0) sh.vmax_part[t][warp & 3] = vm;
@@ -509,133 +386,98 @@ __global__ void __launch_bounds__(kThreads, 1)
         vm = fmaxf(fmaxf(sh.vmax_part[t][0], sh.vmax_part[t][1]), fmaxf(sh.vmax_part[t][2], sh.vmax_part[t][3]));
         o_mult = vm > 0.f ? vm : 1.0f;
         inv_vmax = 1.0f / o_mult;
-        dk_cur = __ldg(dk_row + jlo_t);
-        dv_cur = __ldg(dv_row + jlo_t);
       }
     }
     float m_used = -INFINITY;
     float l_sum = 0.0f;
     bool ok = true;
-    if ((t == 0 || C::kQTm1) && nt > 0) {
-      // Copy this tile's Q rows from shared memory (128-byte swizzle) into its
-      // TMEM columns; the packed words are already in the operand's order.
-      ok = mbar_wait<true>(&sh.q_full, 0, &sh.abort, &g_err_fwd);
-      if (ok) {
-        const uint8_t* src = s_q + t * C::kQTileBytes + r * 128;
-        const uint32_t sw = static_cast<uint32_t>(r & 7);
-        const uint32_t q_col = tmem + lane_base + C::kTmQ + t * C::kQCols;
-#pragma unroll
-        for (int cb = 0; cb < C::kColBlocks; ++cb) {
-          uint32_t w[32];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(src + cb * C::kQBlockBytes + ((c ^ sw) << 4));
-            w[4 * c] = v.x;
-            w[4 * c + 1] = v.y;
-            w[4 * c + 2] = v.z;
-            w[4 * c + 3] = v.w;
-          }
-          tmem_st32(q_col + cb * 32, w);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&sh.q_tm[t]);
-      }
-    }
     for (int u = 0; u < nt; ++u) {
-      const int j = jlo_t + u;  // key block
-      float pmul = 1.0f, dk_nx = 0.f, dv_nx = 0.f;
+      const int j = jlo_t + u;
+      // Scale factors of the two 64-key halves of this block (block-quantised
+      // inputs: K's and V's scale blocks are 64 rows).
+      float c0 = c, c1 = c, pm0 = 1.0f, pm1 = 1.0f;
       if constexpr (BS) {
-        c = cq * dk_cur;
-        pmul = dv_cur * inv_vmax;
-        if (u + 1 < nt) {  // next block's scales, loaded a block ahead
-          dk_nx = __ldg(dk_row + j + 1);
-          dv_nx = __ldg(dv_row + j + 1);
-        }
+        const int b0 = 2 * j, b1 = min(2 * j + 1, n64 - 1);
+        c0 = cq * __ldg(dk_row + b0);
+        c1 = cq * __ldg(dk_row + b1);
+        pm0 = __ldg(dv_row + b0) * inv_vmax;
+        pm1 = __ldg(dv_row + b1) * inv_vmax;
       }
       ok = mbar_wait<true>(&sh.s_full[t], u & 1, &sh.abort, &g_err_fwd);
       if (!ok) break;
       tc_fence_after();
-      float s[kBN];
+      float s0[64], s1[64];
       {
-        uint32_t ra[32], rb[32];
+        uint32_t ra[32], rb[32], rc[32], rd[32];
         tmem_ld32(s_col, ra);
         tmem_ld32(s_col + 32, rb);
+        tmem_ld32(s_col + 64, rc);
+        tmem_ld32(s_col + 96, rd);
         tmem_ld_wait(ra);
         tmem_ld_wait(rb);
+        tmem_ld_wait(rc);
+        tmem_ld_wait(rd);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(ra[i]);
-          s[32 + i] = __uint_as_float(rb[i]);
+          s0[i] = __uint_as_float(ra[i]);
+          s0[32 + i] = __uint_as_float(rb[i]);
+          s1[i] = __uint_as_float(rc[i]);
+          s1[32 + i] = __uint_as_float(rd[i]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&sh.s_free[t]);  // S_t(u+1) may now be written
       const int key0 = j * kBN;
-      // Masked entries: keys after the row (causal), past N, or before the
-      // row's window (key < row - window + 1).
       const bool need_mask = (causal && key0 + kBN - 1 > q0 + t * kBM) || (key0 + kBN > N) ||
                              (WIN && key0 < q0 + t * kBM + kBM - window);
       if (need_mask) {
         const int lim = causal ? min(row_g, N - 1) : N - 1;  // last visible key
-        if constexpr (WIN) {
-          const int lo = row_g - window + 1;  // first visible key
+        const int lo = WIN ? row_g - window + 1 : 0;          // first visible key
 #pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            if (key0 + i > lim || key0 + i < lo) s[i] = -INFINITY;
-        } else {
-#pragma unroll
-          for (int i = 0; i < kBN; ++i)
-            if (key0 + i > lim) s[i] = -INFINITY;
+        for (int i = 0; i < 64; ++i) {
+          if (key0 + i > lim || (WIN && key0 + i < lo)) s0[i] = -INFINITY;
+          if (key0 + 64 + i > lim || (WIN && key0 + 64 + i < lo)) s1[i] = -INFINITY;
         }
       }
-      uint32_t pw[C::kPWords];
-      float row_sum;
+      // Row maximum: four independent chains, then the block's candidate in
+      // log2 units (c0, c1 > 0 preserve the order within each half).
+      float mx[4] = {s0[0], s0[1], s1[0], s1[1]};
+#pragma unroll
+      for (int i = 2; i < 64; i += 2) {
+        mx[0] = fmaxf(mx[0], s0[i]);
+        mx[1] = fmaxf(mx[1], s0[i + 1]);
+        mx[2] = fmaxf(mx[2], s1[i]);
+        mx[3] = fmaxf(mx[3], s1[i + 1]);
+      }
+      const float m_cand = fmaxf(fmaxf(mx[0], mx[1]) * c0, fmaxf(mx[2], mx[3]) * c1);
       float alpha = 1.0f;
       bool raise = false;
-      if (C::kSpecExp && u > 0 && !need_mask) {
-        // Speculative: P with the current reference maximum, computed while the
-        // block maximum is still being found (the two are independent); only a
-        // row whose block maximum exceeds the reference by more than TAU redoes
-        // it with the raised one.
-        row_sum = exp2_pack_row<FP8, C::kEmuGroups, C::kPolyDeg>(s, c, m_used + C::kPShiftLog2, pw);
-        float mx = s[0];
-#pragma unroll
-        for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
-        const float m_cand = mx * c;
-        if (m_cand > m_used + C::kTauLog2) {
-          raise = true;
-          alpha = ex2_approx(m_used - m_cand);
-          m_used = m_cand;
-          row_sum = exp2_pack_row<FP8, C::kEmuGroups, C::kPolyDeg>(s, c, m_used + C::kPShiftLog2, pw);
-        }
-      } else {
-        float mx = s[0];
-#pragma unroll
-        for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
-        const float m_cand = mx * c;
-        if (u == 0) {
-          m_used = m_cand;
-        } else if (m_cand > m_used + C::kTauLog2) {
-          raise = true;
-          alpha = ex2_approx(m_used - m_cand);
-          m_used = m_cand;
-        }
-        // Masked blocks use ex2 throughout, so masked P is exactly 0.  A row
-        // with no visible key so far (only under a window) keeps m = -inf and
-        // takes 0 as the reference here: its p are all 0, and its first
-        // visible key raises m with alpha = 0.
-        const float m_ref = (WIN && m_used == -INFINITY) ? 0.0f : m_used;
-        row_sum = exp2_pack_row<FP8, 0, C::kPolyDeg, BS>(s, c, m_ref + C::kPShiftLog2, pw, pmul);
+      if (u == 0) {
+        m_used = m_cand;
+      } else if (m_cand > m_used + C::kTauLog2) {
+        raise = true;
+        alpha = ex2_approx(m_used - m_cand);
+        m_used = m_cand;
       }
-      l_sum = l_sum * alpha + row_sum;
-      // PV_t(u-1) must be complete before P_t(u) overwrites P_t(u-1) and before
-      // O_t is rescaled.
-      if (u > 0) {
-        ok = mbar_wait<true>(&sh.o_done[t], (u - 1) & 1, &sh.abort, &g_err_fwd);
-        if (!ok) break;
-        tc_fence_after();
+      // A row with no visible key so far (only under a window) keeps m = -inf
+      // and takes 0 as the exponent's reference: its p are all 0.
+      const float m_ref = ((WIN && m_used == -INFINITY) ? 0.0f : m_used) + C::kPShiftLog2;
+      // P over S_t: the first half's words go to the first columns (all of
+      // S_t is in registers by now).
+      float row_sum;
+      {
+        uint32_t pw[C::kPWordsHalf];
+        row_sum = exp2_pack_row<FP8, 0, 3, BS>(s0, c0, m_ref, pw, pm0);
+        if constexpr (FP8) tmem_st16(s_col, pw);
+        else tmem_st32(s_col, pw);
       }
+      {
+        uint32_t pw[C::kPWordsHalf];
+        row_sum += exp2_pack_row<FP8, 0, 3, BS>(s1, c1, m_ref, pw, pm1);
+        if constexpr (FP8) tmem_st16(s_col + 16, pw);
+        else tmem_st32(s_col + 32, pw);
+      }
+      // O_t may be rescaled now: S_t(u) completing means PV_t(u-1), issued
+      // before it, is complete too (done after P, when S is no longer held
+      // in registers).
       if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
@@ -647,15 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(o_col + cc, rr);
         }
       }
-      if constexpr (FP8) tmem_st16(p_col, pw);
-      else tmem_st32(p_col, pw);
+      l_sum = l_sum * alpha + row_sum;
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sh.p_full[t]);
-      if constexpr (BS) {
-        dk_cur = dk_nx;
-        dv_cur = dv_nx;
-      }
     }
     // Epilogue: O = O~ / l in bf16, staged with the 128-byte swizzle in this
     // tile's own Q space and written by TMA stores, which drop box rows past N.
@@ -669,19 +506,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       const float inv = o_mult / l_sum;
-      uint8_t* stage = s_q + t * C::kQTileBytes;
+      uint8_t* stage = s_q + t * C::kTileBytes;
       const uint32_t sw = static_cast<uint32_t>(r & 7);
       const bool leader = r == 0;
 #pragma unroll 1
       for (int ob = 0; ob < C::kOColBlocks; ob += C::kOStageBlocks) {
-        if (ob > 0) {  // the staging space is reused: earlier stores must have read it
+        if (ob > 0) {
           if (leader) bulk_wait_read_all();
           named_bar_sync(1 + t, kBM);
         }
         if (ok) {
 #pragma unroll
           for (int b = 0; b < C::kOStageBlocks; ++b) {
-            uint8_t* row_base = stage + b * C::kQBlockBytes + r * 128;
+            uint8_t* row_base = stage + b * C::kBlockBytes + r * 128;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               uint32_t rr[32];
@@ -703,11 +540,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && leader) {
 #pragma unroll
           for (int b = 0; b < C::kOStageBlocks; ++b)
-            tma_store_3d(&map_o, (ob + b) * 64, q0 + t * kBM, bh, stage + b * C::kQBlockBytes);
+            tma_store_3d(&map_o, (ob + b) * 64, q0 + t * kBM, bh, stage + b * C::kBlockBytes);
           bulk_commit_group();
         }
       }
-      if (leader) bulk_wait_read_all();  // shared memory must outlive the stores' reads
+      if (leader) bulk_wait_read_all();
       if (ok && row_g < N)
         out_lse[static_cast<size_t>(bh) * N + row_g] = (m_used + C::kPShiftLog2) * 0.69314718055994531f + logf(l_sum);
     }
@@ -737,16 +574,12 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
     return FA_ERR_LAUNCH;
   dim3 grid(static_cast<unsigned>(((a.N + 2 * kBM - 1) / (2 * kBM)) * BH));
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  // Query heads per group: the keys and values their blocks stream should
-  // stay within about 32 MB of the L2 (query heads of one key/value head
-  // share it).
   const int qgroup = a.H / a.Hkv;
   const long long kv_bytes_per_qhead = 2ll * a.N * D * C::kElemBytes / qgroup;
   int group = static_cast<int>(std::max<long long>(1, (32ll << 20) / std::max<long long>(1, kv_bytes_per_qhead)));
   group = std::min(group, BH);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a.lse, a.descale_q,
-                                                   a.descale_k, a.descale_v, BH, a.N, a.causal, scale_log2, a.H,
-                                                   qgroup, a.window, group);
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a.lse, a.descale_q, a.descale_k, a.descale_v, BH,
+                                                   a.N, a.causal, scale_log2, a.H, qgroup, a.window, group);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

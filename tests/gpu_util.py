@@ -51,8 +51,9 @@ def half_ulp_bf16(x):
 def o_tight_bound(o_ref, o_absv_ref, n_keys):
     """Per-element bound on |O - O_ref| for the bf16 forward, from its
     arithmetic, with o_absv_ref = P|V| (the oracle's output for |V|):
-      * P is rounded to bf16 before P V while l sums the unrounded p: the
-        error of O~/l is at most 2^-9 sum_j P_ij |V_jk| = 2^-9 (P|V|)_ik;
+      * P is rounded to bf16 (8 significant bits, unit roundoff 2^-8) before
+        P V while l sums the unrounded p: the error of O~/l is at most
+        2^-8 sum_j P_ij |V_jk| = 2^-8 (P|V|)_ik;
       * S = Q K^T in fp32 from exact bf16 products (d terms): an absolute
         error of at most about 2^-13 relative in each p, which moves O by at
         most 2^-11 (P|V|);
@@ -63,7 +64,7 @@ def o_tight_bound(o_ref, o_absv_ref, n_keys):
     The bound has no global max|V| term, so it is tight where |O| and P|V|
     are small: a wrongly masked or unmasked key, or P rounded the wrong way,
     shows."""
-    coef = 2.0 ** -9 + 2.0 ** -11 + n_keys * 2.0 ** -23
+    coef = 2.0 ** -8 + 2.0 ** -11 + n_keys * 2.0 ** -23
     pre = coef * np.asarray(o_absv_ref, dtype=np.float64)
     return pre + half_ulp_bf16(np.abs(np.asarray(o_ref, dtype=np.float64)) + pre) + 2.0 ** -24
 
