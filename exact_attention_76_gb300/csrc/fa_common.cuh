@@ -386,6 +386,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input max, sm_100 and later).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x for two values on the FMA pipes (no special-function unit): Cody-Waite
 // reduction x = n + f, n = round(x) by the 1.5 * 2^23 shifter, f in [-1/2, 1/2];
 // 2^f by the degree-DEG polynomial of least maximum relative error on that
