@@ -89,7 +89,7 @@ __global__ void timeout_probe_kernel(long long limit_cycles) {
 }  // namespace
 
 bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, int cols, int N, int BH, int box_cols,
-                     int box_rows) {
+                     int box_rows, int swizzle_bytes) {
   EncodeTiledFn enc = resolve_encode();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(N),
@@ -101,9 +101,9 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, int col
   const CUtensorMapDataType dt = elem_bytes == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUtensorMapSwizzle swz = swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Special-function-unit rate: every thread runs 8 independent chains
@@ -320,7 +320,6 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
   if ((st = check_ptrs(q8, k8, v8, o, lse)) != FA_OK) return st;
   if (descale_q == nullptr || descale_k == nullptr || descale_v == nullptr) return FA_ERR_INVALID_ARG;
   if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((st = check_device()) != FA_OK) return st;
@@ -335,7 +334,6 @@ fa_status fa_fwd_fp8_blocks(const void* q8, const void* k8, const void* v8, cons
   if ((st = check_ptrs(q8, k8, v8, o, lse)) != FA_OK) return st;
   if (descale_q == nullptr || descale_k == nullptr || descale_v == nullptr) return FA_ERR_INVALID_ARG;
   if ((st = check_shape(B, H, N, d)) != FA_OK) return st;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
   if ((st = check_scale(scale)) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if ((st = check_device()) != FA_OK) return st;

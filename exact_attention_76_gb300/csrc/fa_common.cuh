@@ -6,7 +6,8 @@
 //  * Tiles of 128 rows are staged in shared memory by TMA with the 128-byte
 //    swizzle: each row holds 128 bytes (64 bf16 or 128 e4m3 values), 8 rows
 //    form a 1024-byte swizzle atom, and a wider row is split into 128-byte
-//    column blocks stored one after the other.
+//    column blocks stored one after the other.  A 64-byte row (64 e4m3
+//    values) uses the 64-byte swizzle in the same way (512-byte atoms).
 //  * The MMA accumulator for M = 128 keeps row i in TMEM lane i; warp w of a
 //    warpgroup reads lanes 32*(w%4) .. 32*(w%4)+31.
 //  * Every wait on an mbarrier is bounded: past the limit the waiting thread
@@ -265,23 +266,27 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand.
-//   K-major operand: sbo = byte distance between 8-row groups (1024 for dense
-//                    tiles); lbo is not used by the hardware (set to 16).
-//   MN-major operand: lbo = byte distance between consecutive 128-byte column
+// Shared-memory matrix descriptor for an operand stored with the 128-byte
+// (or 64-byte) swizzle: rows of `swz` bytes, 8 rows to a swizzle atom.
+//   K-major operand: sbo = byte distance between 8-row groups (8 * swz for
+//                    dense tiles); lbo is not used by the hardware (set to 16).
+//   MN-major operand: lbo = byte distance between consecutive swz-byte column
 //                    blocks along M/N; sbo = byte distance between 8-row groups
 //                    along K.
 // Fields: start address >> 4 (bits 0-13), lbo >> 4 (16-29), sbo >> 4 (32-45),
-// the fixed descriptor version 1 (bits 46-47), base offset 0, swizzle mode 2 =
-// 128-byte (bits 61-63).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// the fixed descriptor version 1 (bits 46-47), base offset 0, layout type
+// (bits 61-63): 2 = 128-byte swizzle, 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_sw(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
-  d |= 2ull << 61;
+  d |= (swz == 64 ? 4ull : 2ull) << 61;
   return d;
+}
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return sdesc_sw(saddr, lbo, sbo, 128);
 }
 
 // Descriptor of the same operand layout starting `byte_off` bytes further:

@@ -143,12 +143,20 @@ template <int D, bool FP8>
 struct FwdCfg {
   static constexpr int kElemBytes = FP8 ? 1 : 2;
   static constexpr int kRowBytes = D * kElemBytes;
-  static constexpr int kColBlocks = kRowBytes / 128;
-  static constexpr int kBoxCols = 128 / kElemBytes;
-  static constexpr int kBlockBytes = 128 * 128;          // one 128-row x 128-byte column block
+  // Swizzle width of Q, K and V in shared memory: 128 bytes, or 64 when a row
+  // is 64 bytes (e4m3 at d = 64).
+  static constexpr int kSwz = kRowBytes >= 128 ? 128 : 64;
+  static constexpr int kColBlocks = kRowBytes / kSwz;     // kSwz-byte column blocks
+  static constexpr int kBoxCols = kSwz / kElemBytes;
+  static constexpr int kBlockBytes = 128 * kSwz;         // one 128-row column block
+  static constexpr int kStepsPerBlock = kSwz / 32;       // K steps of 32 bytes per column block
   static constexpr int kTileBytes = 128 * kRowBytes;     // a Q tile or a K / V block
+  // O (bf16, 128-byte swizzle) is staged in the tile's Q space: kORows rows
+  // of kOStageBlocks 128-byte column blocks at a time.
   static constexpr int kOColBlocks = D * 2 / 128;
-  static constexpr int kOStageBlocks = kTileBytes / kBlockBytes;
+  static constexpr int kORows = kTileBytes / 128 >= 128 ? 128 : kTileBytes / 128;
+  static constexpr int kOStageBytes = kORows * 128;     // one staged column block
+  static constexpr int kOStageBlocks = kTileBytes / kOStageBytes;
   static constexpr int kSlotsFit = (232448 - 1024 - 1024 - 2 * kTileBytes) / kTileBytes;
   static constexpr int kSlots = kSlotsFit > 16 ? 16 : kSlotsFit;
   static constexpr int kSmemBytes = 2 * kTileBytes + kSlots * kTileBytes + 1024;
@@ -172,7 +180,9 @@ struct FwdCfg {
   static constexpr uint32_t kTmO = 256;   // + t * D
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(kSlots >= 4, "K/V ring depth");
-  static_assert(kOStageBlocks >= 1 && kOColBlocks % kOStageBlocks == 0, "O staging");
+  static_assert(kOStageBlocks >= 1 && (kOColBlocks % kOStageBlocks == 0 || kOStageBlocks > kOColBlocks),
+                "O staging");
+  static_assert(kORows == 128 || kORows == 64, "O staging rows");
   static_assert(kSmemBytes <= 232448 - 1024, "shared memory budget");
 };
 
@@ -286,15 +296,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one() && n_max > 0) {
-      const uint64_t q_desc = sdesc_sw128(smem_u32(s_q), 16, 1024);                  // K-major Q tiles
-      const uint64_t k_desc = sdesc_sw128(smem_u32(s_kv), 16, 1024);                 // K-major K slots
-      const uint64_t v_desc = sdesc_sw128(smem_u32(s_kv), C::kBlockBytes, 1024);     // MN-major V slots
+      const uint64_t q_desc = sdesc_sw(smem_u32(s_q), 16, 8 * C::kSwz, C::kSwz);               // K-major Q
+      const uint64_t k_desc = sdesc_sw(smem_u32(s_kv), 16, 8 * C::kSwz, C::kSwz);              // K-major K
+      const uint64_t v_desc = sdesc_sw(smem_u32(s_kv), C::kBlockBytes, 8 * C::kSwz, C::kSwz);  // MN-major V
       auto issue_s = [&](int t, int slot) {
         const uint64_t a0 = sdesc_advance(q_desc, t * C::kTileBytes);
         const uint64_t b0 = sdesc_advance(k_desc, slot * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < C::kQKSteps; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+          const uint32_t off = (kk / C::kStepsPerBlock) * C::kBlockBytes + (kk % C::kStepsPerBlock) * 32;
           issue_mma(FP8, tmem + C::kTmS + t * kBN, sdesc_advance(a0, off), sdesc_advance(b0, off), C::kIdescS,
                     kk > 0);
         }
@@ -306,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tm = tmem + C::kTmO + t * D;
 #pragma unroll
         for (int kk = 0; kk < C::kPVSteps; ++kk)
-          issue_mma_ts(FP8, d_tm, a_tm + kk * 8, sdesc_advance(b0, kk * C::kKPerMma * 128), C::kIdescPV,
+          issue_mma_ts(FP8, d_tm, a_tm + kk * 8, sdesc_advance(b0, kk * C::kKPerMma * C::kSwz), C::kIdescPV,
                        (acc || kk > 0) ? 1u : 0u);
         tc_commit(&sh.o_done[t]);
       };
@@ -521,41 +531,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float inv = o_mult / l_sum;
       uint8_t* stage = s_q + t * C::kTileBytes;
-      const uint32_t sw = static_cast<uint32_t>(r & 7);
+      const int ro = r % C::kORows;  // row within a staged group
+      const uint32_t sw = static_cast<uint32_t>(ro & 7);
       const bool leader = r == 0;
+      constexpr int kStage = C::kOStageBlocks < C::kOColBlocks ? C::kOStageBlocks : C::kOColBlocks;
+      int round = 0;
 #pragma unroll 1
-      for (int ob = 0; ob < C::kOColBlocks; ob += C::kOStageBlocks) {
-        if (ob > 0) {
-          if (leader) bulk_wait_read_all();
-          named_bar_sync(1 + t, kBM);
-        }
-        if (ok) {
-#pragma unroll
-          for (int b = 0; b < C::kOStageBlocks; ++b) {
-            uint8_t* row_base = stage + b * C::kBlockBytes + r * 128;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t rr[32];
-              tmem_ld32(o_col + (ob + b) * 64 + h * 32, rr);
-              tmem_ld_wait(rr);
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<uint4*>(row_base + (((h * 4 + i) ^ sw) << 4)) =
-                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
+      for (int rg = 0; rg < kBM / C::kORows; ++rg) {
+#pragma unroll 1
+        for (int ob = 0; ob < C::kOColBlocks; ob += kStage, ++round) {
+          if (round > 0) {  // the staging space is reused: earlier stores must have read it
+            if (leader) bulk_wait_read_all();
+            named_bar_sync(1 + t, kBM);
           }
-          fence_proxy_async_smem();
-        }
-        ok = named_bar_and(1 + t, kBM, ok);
-        if (ok && leader) {
+          if (ok && r / C::kORows == rg) {
 #pragma unroll
-          for (int b = 0; b < C::kOStageBlocks; ++b)
-            tma_store_3d(&map_o, (ob + b) * 64, q0 + t * kBM, bh, stage + b * C::kBlockBytes);
-          bulk_commit_group();
+            for (int b = 0; b < kStage; ++b) {
+              uint8_t* row_base = stage + b * C::kOStageBytes + ro * 128;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t rr[32];
+                tmem_ld32(o_col + (ob + b) * 64 + h * 32, rr);
+                tmem_ld_wait(rr);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv, __uint_as_float(rr[2 * i + 1]) * inv);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  *reinterpret_cast<uint4*>(row_base + (((h * 4 + i) ^ sw) << 4)) =
+                      make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              }
+            }
+            fence_proxy_async_smem();
+          }
+          ok = named_bar_and(1 + t, kBM, ok);
+          if (ok && leader) {
+#pragma unroll
+            for (int b = 0; b < kStage; ++b)
+              tma_store_3d(&map_o, (ob + b) * 64, q0 + t * kBM + rg * C::kORows, bh, stage + b * C::kOStageBytes);
+            bulk_commit_group();
+          }
         }
       }
       if (leader) bulk_wait_read_all();
@@ -578,10 +594,10 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   const int BH = a.B * a.H;
   const int BHkv = a.B * a.Hkv;
   CUtensorMap mq, mk, mv, mo;
-  if (!encode_rows_map(&mq, a.q, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBM) ||
-      !encode_rows_map(&mo, a.o, 2, D, a.N, BH, 64, kBM) ||
-      !encode_rows_map(&mk, a.k, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN) ||
-      !encode_rows_map(&mv, a.v, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN))
+  if (!encode_rows_map(&mq, a.q, C::kElemBytes, D, a.N, BH, C::kBoxCols, kBM, C::kSwz) ||
+      !encode_rows_map(&mo, a.o, 2, D, a.N, BH, 64, C::kORows) ||
+      !encode_rows_map(&mk, a.k, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN, C::kSwz) ||
+      !encode_rows_map(&mv, a.v, C::kElemBytes, D, a.N, BHkv, C::kBoxCols, kBN, C::kSwz))
     return FA_ERR_LAUNCH;
   auto kern = fa_fwd_kernel<D, FP8, BS, WIN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
@@ -608,11 +624,13 @@ fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream) {
 }
 
 fa_status launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
-  return launch_fwd_impl<128, true, false, false>(a, stream);
+  return a.d == 64 ? launch_fwd_impl<64, true, false, false>(a, stream)
+                   : launch_fwd_impl<128, true, false, false>(a, stream);
 }
 
 fa_status launch_fwd_fp8_blocks(const FwdArgs& a, cudaStream_t stream) {
-  return launch_fwd_impl<128, true, true, false>(a, stream);
+  return a.d == 64 ? launch_fwd_impl<64, true, true, false>(a, stream)
+                   : launch_fwd_impl<128, true, true, false>(a, stream);
 }
 
 uint32_t fwd_bf16_take_error(cudaStream_t s) {

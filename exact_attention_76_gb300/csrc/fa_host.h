@@ -13,9 +13,10 @@ namespace fa {
 
 // Encodes a 3-D tiled map over a [BH, N, cols] row-major tensor of
 // `elem_bytes`-byte elements with a box of (box_cols x box_rows x 1) and the
-// 128-byte swizzle.  Rows past N read as zeros.  Returns false on failure.
+// 128-byte swizzle (64-byte when swizzle_bytes is 64; the box row must then be
+// 64 bytes).  Rows past N read as zeros.  Returns false on failure.
 bool encode_rows_map(CUtensorMap* map, const void* base, int elem_bytes, int cols, int N, int BH, int box_cols,
-                     int box_rows);
+                     int box_rows, int swizzle_bytes = 128);
 
 struct FwdArgs {
   const void* q;

@@ -143,7 +143,8 @@ fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, 
 /*
  * FP8 forward ("FLASH-ATTN", FlashAttention-3 > Low-precision with FP8:
  * per-tensor scaling keeps one scalar per tensor).
- *   q8, k8, v8 : [B,H,N,d] e4m3 codes (1 byte each); X = delta_X * code.
+ *   q8, k8, v8 : [B,H,N,d] e4m3 codes (1 byte each), d in {64, 128};
+ *                X = delta_X * code.
  *   descale_q, descale_k, descale_v : DEVICE pointers to one fp32 each (delta).
  *   o   : [B,H,N,d] bf16 out, O = softmax(scale * (dq dk) q8 k8^T) (dv v8).
  *   lse : [B,H,N] fp32 out, natural-log LogSumExp of the scaled logits.
@@ -203,7 +204,7 @@ fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void*
  * of B_r x d or B_c x d rows quantised each with its own scale; the kernel,
  * which works block by block, scales each block of S by the scales of its Q
  * and K blocks).
- *   q8, k8, v8 : [B,H,N,d] e4m3 codes, d = 128.
+ *   q8, k8, v8 : [B,H,N,d] e4m3 codes, d in {64, 128}.
  *   descale_q  : DEVICE [B*H, ceil(N/128)] fp32, the scale of rows
  *                [128 b, 128 b + 128) of each head of Q.
  *   descale_k, descale_v : DEVICE [B*H, ceil(N/64)] fp32, per 64 rows of K

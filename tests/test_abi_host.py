@@ -91,7 +91,7 @@ def test_bwd_argument_errors_before_any_launch(lib):
 def test_fp8_argument_errors_before_any_launch(lib):
     p = ALIGNED
     assert lib.fa_fwd_fp8(p, p, p, None, p, p, p, p, 1, 1, 128, 128, 0, 0.1, None) == 1
-    assert lib.fa_fwd_fp8(p, p, p, p, p, p, p, p, 1, 1, 128, 64, 0, 0.1, None) == 2
+    assert lib.fa_fwd_fp8(p, p, p, p, p, p, p, p, 1, 1, 128, 96, 0, 0.1, None) == 2
     assert lib.fa_fwd_fp8(p, p, p + 1, p, p, p, p, p, 1, 1, 128, 128, 0, 0.1, None) == 3
 
 

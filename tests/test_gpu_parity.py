@@ -197,10 +197,11 @@ def test_window_many_items():
     assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_forward_many_items(causal):
+def test_fp8_forward_many_items(causal, d):
     # 3 * 64 = 192 items; against exact attention on the dequantised inputs
-    orig, codes, deltas, o, lse, scale = _fp8_case(640, causal, B=1, H=64)
+    orig, codes, deltas, o, lse, scale = _fp8_case(640, causal, B=1, H=64, d=d)
     deq = [oracle.dequantize_e4m3(c, dl) for c, dl in zip(codes, deltas)]
     o_deq, l_deq = oracle.forward(*deq, causal, scale)
     e = rel_fro(f64(o), o_deq)
@@ -255,12 +256,13 @@ def _fp8_case(N, causal, seed=4, B=1, H=2, d=128):
     return (q, k, v), codes, deltas, o, lse, scale
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [256, 1000])
-def test_fp8_forward_kernel_error(causal, N):
+def test_fp8_forward_kernel_error(causal, N, d):
     # Against exact attention on the dequantised e4m3 inputs: what remains is
     # the kernel's own error (P stored as e4m3, fp32 accumulation).
-    orig, codes, deltas, o, lse, scale = _fp8_case(N, causal)
+    orig, codes, deltas, o, lse, scale = _fp8_case(N, causal, d=d)
     deq = [oracle.dequantize_e4m3(c, dl) for c, dl in zip(codes, deltas)]
     o_deq, l_deq = oracle.forward(*deq, causal, scale)
     e = rel_fro(f64(o), o_deq)
@@ -277,6 +279,34 @@ def test_fp8_forward_vs_unquantised_per_tensor_only(causal):
     o_ref, _ = oracle.forward_fp8_reference(*orig, causal, scale)
     e = rel_fro(f64(o), o_ref)
     assert e <= FP8_O_REL_FRO, f"FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
+
+
+# The FP8 gate (6e-2 relative Frobenius against exact attention on the
+# unquantised inputs) is the d = 128 FP8 workload's.  At d = 64 a Hadamard
+# rotation spreads an outlier over half as many coordinates, and e4m3 storage
+# of the x10-outlier inputs alone already costs up to 6.8 % (measured in
+# float64 on the oracle's own quantised inputs): there the GPU's total error is
+# bounded by that storage error plus the kernel's own share, at most 2 %.
+FP8_KERNEL_SHARE = 2e-2
+
+
+def _fp8_unquantised_bound(q, k, v, causal, scale, d, rotate_qk, block_rows=None):
+    if d == 128:
+        return FP8_O_REL_FRO
+    o_ref, _ = oracle.forward_fp8_reference(q, k, v, causal, scale)
+    deq = []
+    for t, rot, br in ((q, rotate_qk, block_rows[0] if block_rows else None),
+                       (k, rotate_qk, block_rows[1] if block_rows else None),
+                       (v, False, block_rows[2] if block_rows else None)):
+        y = oracle.rotate_rows(t) if rot else f64(t)
+        if br is None:
+            c, dl = oracle.quantize_e4m3_reference(y)
+            deq.append(oracle.dequantize_e4m3(c, float(np.float32(dl))))
+        else:
+            c, dl = oracle.quantize_e4m3_blocks_reference(y, br)
+            deq.append(oracle.dequantize_e4m3_blocks(c, dl.astype(np.float32).astype(np.float64), br))
+    o_q, _ = oracle.forward(*deq, causal, scale)
+    return rel_fro(o_q, o_ref) + FP8_KERNEL_SHARE
 
 
 def _e4m3_codes(t):
@@ -305,12 +335,13 @@ def test_fp8_quantize_matches_reference(hadamard, d, dtype):
     assert (got == ref_codes).mean() > 0.999
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [256, 1000])
-def test_fp8_forward_with_incoherent_processing(causal, N):
+def test_fp8_forward_with_incoherent_processing(causal, N, d):
     # Q and K rotated by the Hadamard transform before per-tensor e4m3
     # storage (V as is), against exact attention on the unquantised inputs.
-    B, H, d = 1, 2, 128
+    B, H = 1, 2
     q, k, v = inputs.draw_outlier_fp32(B, H, N, d, seed=4)
     scale = 1 / math.sqrt(d)
     q8, dsq = api.fa_fp8_quantize(q.cuda(), True)
@@ -320,7 +351,8 @@ def test_fp8_forward_with_incoherent_processing(causal, N):
     torch.cuda.synchronize()
     o_ref, l_ref = oracle.forward_fp8_reference(q, k, v, causal, scale)
     e = rel_fro(f64(o), o_ref)
-    assert e <= FP8_O_REL_FRO, f"FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
+    bound = _fp8_unquantised_bound(q, k, v, causal, scale, d, True)
+    assert e <= bound, f"FP8 O rel-Frobenius vs unquantised inputs {e:.3e} (bound {bound:.3e})"
 
 
 # ---------------------------------------------------------------- FP8, block quantisation
@@ -358,12 +390,13 @@ def _block_scaled_inputs(B, H, N, d, seed):
     return out
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [256, 1000])
-def test_fp8_blocks_forward_kernel_error(causal, N):
+def test_fp8_blocks_forward_kernel_error(causal, N, d):
     # Against exact attention on the dequantised block-quantised inputs: what
     # remains is the kernel's own error (P as e4m3, fp32 accumulation).
-    B, H, d = 1, 2, 128
+    B, H = 1, 2
     q, k, v = _block_scaled_inputs(B, H, N, d, seed=4)
     scale = 1 / math.sqrt(d)
     cq, dq = oracle.quantize_e4m3_blocks_reference(q, api.FP8_BLOCK_Q)
@@ -381,11 +414,12 @@ def test_fp8_blocks_forward_kernel_error(causal, N):
     assert max_abs(f64(lse), l_ref) <= 2e-2
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_blocks_forward_with_incoherent_processing(causal):
+def test_fp8_blocks_forward_with_incoherent_processing(causal, d):
     # The whole FP8 path on the GPU: Hadamard-rotated Q and K and plain V stored
     # per block, against exact attention on the unquantised inputs.
-    B, H, N, d = 1, 2, 1000, 128
+    B, H, N = 1, 2, 1000
     q, k, v = inputs.draw_outlier_fp32(B, H, N, d, seed=4)
     scale = 1 / math.sqrt(d)
     q8, dsq = api.fa_fp8_quantize_blocks(q.cuda(), True, api.FP8_BLOCK_Q)
@@ -395,7 +429,9 @@ def test_fp8_blocks_forward_with_incoherent_processing(causal):
     torch.cuda.synchronize()
     o_ref, l_ref = oracle.forward_fp8_reference(q, k, v, causal, scale)
     e = rel_fro(f64(o), o_ref)
-    assert e <= FP8_O_REL_FRO, f"block FP8 O rel-Frobenius vs unquantised inputs {e:.3e}"
+    bound = _fp8_unquantised_bound(q, k, v, causal, scale, d, True,
+                                   (api.FP8_BLOCK_Q, api.FP8_BLOCK_KV, api.FP8_BLOCK_KV))
+    assert e <= bound, f"block FP8 O rel-Frobenius vs unquantised inputs {e:.3e} (bound {bound:.3e})"
 
 
 # ---------------------------------------------------------------- sliding window
