@@ -60,6 +60,20 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+
+// Lets the next kernel of the stream, when it is launched with programmatic
+// stream serialization, begin launching once every CTA of this grid has
+// executed this (its CTAs then take SMs as this grid's CTAs exit).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their memory
+// operations are visible; returns at once when the grid was launched without
+// programmatic stream serialization.  Every access to memory that an earlier
+// kernel of the stream reads or writes comes after this.
+__device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -258,6 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+  // Set-up done: the next kernel may start launching; inputs are read only
+  // after the kernels before this one have completed.
+  pdl_launch_dependents();
+  pdl_wait_prior();
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -608,9 +612,10 @@ fa_status launch_fwd_impl(const FwdArgs& a, cudaStream_t stream) {
   const long long kv_bytes_per_qhead = 2ll * a.N * D * C::kElemBytes / qgroup;
   int group = static_cast<int>(std::max<long long>(1, (32ll << 20) / std::max<long long>(1, kv_bytes_per_qhead)));
   group = std::min(group, BH);
-  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, mo, a.lse, a.descale_q, a.descale_k, a.descale_v, BH,
-                                                   a.N, a.causal, scale_log2, a.H, qgroup, a.window, group);
-  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), C::kSmemBytes, stream, mq, mk, mv, mo, a.lse,
+                                   a.descale_q, a.descale_k, a.descale_v, BH, a.N, a.causal, scale_log2, a.H, qgroup,
+                                   a.window, group);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 }  // namespace
