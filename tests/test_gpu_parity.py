@@ -669,3 +669,36 @@ def test_exp2_polynomial_on_the_gpu(degree, bound):
     # below the range the result stands in for zero
     tiny = f64(api.fa_debug_exp2_poly(torch.tensor([-np.inf, -1000.0, -126.0], device="cuda"), degree))
     assert np.all(tiny > 0) and np.all(tiny <= 2.0 ** -125)
+
+
+# ---------------------------------------------------------------- back-to-back dependent calls
+
+def test_back_to_back_calls_read_the_previous_output():
+    # The forward and backward main kernels start launching while the kernel
+    # before them finishes and wait for it before touching memory.  Chains of
+    # small launch-bound calls where each reads the previous call's output
+    # (O of one forward is Q of the next; the backward reads that forward's O
+    # and L) must give what the oracle gives for the same chain.
+    B, H, N, d, scale = 1, 2, 192, 64, 0.125
+    q, k, v, do = inputs.draw_bf16(B, H, N, d, seed=31)
+    qd, kd, vd, dod = to_dev(q, k, v, do)
+    x = qd
+    for _ in range(6):
+        o, lse = api.fa_fwd(x, kd, vd, True, scale)
+        x = o
+    dq, dk, dv = api.fa_bwd(x, kd, vd, *api.fa_fwd(x, kd, vd, True, scale), dod, True, scale)
+    torch.cuda.synchronize()
+    xr = q
+    for _ in range(6):
+        xr = torch.from_numpy(oracle.forward(xr, k, v, True, scale)[0]).to(torch.bfloat16)
+    # each step's input is the GPU's previous bf16 output: compare the last
+    # step against the oracle on that same input
+    o_ref, l_ref = oracle.forward(x.cpu(), k, v, True, scale)
+    o_last, l_last = api.fa_fwd(x, kd, vd, True, scale)
+    torch.cuda.synchronize()
+    assert max_abs(f64(o_last), o_ref) <= O_MAX_ABS
+    assert max_abs(f64(l_last), l_ref) <= L_MAX_ABS
+    # the chain itself stays close to the oracle's chain: each of its six
+    # steps may add up to the O gate (bf16 rounding of its output)
+    assert max_abs(f64(x), f64(xr)) <= 6 * O_MAX_ABS
+    check_bwd(dq, dk, dv, x.cpu(), k, v, do, True, scale)
