@@ -98,8 +98,29 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __r
                                                                 float scale) {
   pdl_launch_dependents();
   pdl_wait_prior();
+  // Groups of 8 values; each thread keeps four groups' loads in flight before
+  // converting and storing them.
+  constexpr int kU = 4;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+  long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + (kU - 1) * stride < n8; i += kU * stride) {
+    float4 a[kU], b[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      a[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * (i + u * stride));
+      b[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * (i + u * stride) + 1);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      uint4 r;
+      r.x = pack_bf16x2(a[u].x * scale, a[u].y * scale);
+      r.y = pack_bf16x2(a[u].z * scale, a[u].w * scale);
+      r.z = pack_bf16x2(b[u].x * scale, b[u].y * scale);
+      r.w = pack_bf16x2(b[u].z * scale, b[u].w * scale);
+      reinterpret_cast<uint4*>(dq)[i + u * stride] = r;
+    }
+  }
+  for (; i < n8; i += stride) {
     const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
     const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
     uint4 r;

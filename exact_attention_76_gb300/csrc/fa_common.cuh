@@ -121,6 +121,19 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (never suspends).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Per-CTA cancellation state shared by all roles of a kernel.
 struct CtaAbort {
   volatile int flag;
@@ -137,6 +150,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, CtaAbo
   const long long t0 = clock64();
   while (true) {
     if (kSuspend ? mbar_try_wait_suspend(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
+    if (ab->flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      atomicOr(err, FA_DEVERR_TIMEOUT);
+      ab->flag = 1;
+      return false;
+    }
+  }
+}
+
+// As mbar_wait, polling with mbar_test_wait: the thread is never suspended,
+// so it sees the phase complete sooner, at the cost of issue slots.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, CtaAbort* ab, uint32_t* err) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test_wait(bar, parity)) return true;
     if (ab->flag) return false;
     if (clock64() - t0 > kWaitLimitCycles) {
       atomicOr(err, FA_DEVERR_TIMEOUT);

@@ -350,7 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = wait_load(v_idx);
               v_ready = true;
             }
-            ok = ok && mbar_wait<true>(&sh.p_full[t], u & 1, &sh.abort, &g_err_fwd);
+            // bf16 at d = 128 polls for P (+0.3 % causal, +1.7 % without a mask,
+            // measured); elsewhere the suspending wait measured as fast or faster
+            // (FP8: polling -3 %).
+            ok = ok && ((!FP8 && D == 128) ? mbar_wait_poll(&sh.p_full[t], u & 1, &sh.abort, &g_err_fwd)
+                                           : mbar_wait<true>(&sh.p_full[t], u & 1, &sh.abort, &g_err_fwd));
             if (!ok) break;
             tc_fence_after();
             issue_pv(t, v_idx % C::kSlots, u > 0);
