@@ -29,7 +29,9 @@
 // one warpgroup's softmax overlaps the other tile's two products (the
 // ping-pong of two consumer warpgroups, "FLASH-ATTN", FlashAttention-3).  A
 // completed S_t(j) also means that PV_t(j-1), issued before it, is complete,
-// so the warpgroup may rescale O_t right after reading S_t(j).
+// so the warpgroup may rescale O_t right after reading S_t(j).  In bf16 P is
+// handed over in two 64-key halves: PV over the first half runs while the
+// warpgroup exponentiates the second.
 //
 // Softmax works in the log2 domain: x = S * (scale * log2 e) with one FMA, then
 // ex2.  The reference maximum m_used is raised only when a block's maximum
@@ -166,6 +168,12 @@ struct FwdCfg {
   static constexpr float kTauLog2 = FP8 ? 4.0f : 8.0f;
   static constexpr float kPShiftLog2 = FP8 ? -4.0f : 0.0f;
   static constexpr int kPWordsHalf = FP8 ? 16 : 32;      // TMEM words of P per 64 keys
+  // P handed to the MMA thread in two 64-key halves, so that PV over the
+  // first half runs while the second half is exponentiated: measured +4 %
+  // (causal) and +6 % (no mask) at bf16 d = 128, +1 % at d = 64; e4m3 (whose
+  // PV half is only 128 tensor cycles) measured 1-2.5 % slower and hands P
+  // over whole.
+  static constexpr bool kSplitP = !FP8;
   // Exponentials on the FMA pipes ("software exp2"): groups of four, of the
   // 16 per 64 keys, taken by the polynomial exp2 of fa_common.cuh, and its
   // degree (bf16 P keeps 8 significant bits, e4m3 P 4).  Measured on GB300,
@@ -192,6 +200,7 @@ struct FwdSmem {
   uint64_t kv_empty[16];
   uint64_t s_full[2];
   uint64_t p_full[2];
+  uint64_t p_half[2];
   uint64_t o_done[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -248,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sh.s_full[t], 1);
       mbar_init(&sh.p_full[t], kBM);
+      mbar_init(&sh.p_half[t], kBM);
       mbar_init(&sh.o_done[t], 1);
     }
     mbar_init(&sh.drain, 1);
@@ -314,15 +324,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(&sh.s_full[t]);
       };
-      auto issue_pv = [&](int t, int slot, bool acc) {
+      // O_t += P_t V_j over the K steps [k0, k1) of the block (P over S_t).
+      auto issue_pv = [&](int t, int slot, bool acc, int k0, int k1) {
         const uint64_t b0 = sdesc_advance(v_desc, slot * C::kTileBytes);
-        const uint32_t a_tm = tmem + C::kTmS + t * kBN;  // P over S_t
+        const uint32_t a_tm = tmem + C::kTmS + t * kBN;
         const uint32_t d_tm = tmem + C::kTmO + t * D;
 #pragma unroll
-        for (int kk = 0; kk < C::kPVSteps; ++kk)
+        for (int kk = k0; kk < k1; ++kk)
           issue_mma_ts(FP8, d_tm, a_tm + kk * 8, sdesc_advance(b0, kk * C::kKPerMma * C::kSwz), C::kIdescPV,
                        (acc || kk > 0) ? 1u : 0u);
-        tc_commit(&sh.o_done[t]);
+      };
+      // bf16 at d = 128 polls for P (+0.3 % causal, +1.7 % without a mask,
+      // measured); elsewhere the suspending wait measured as fast or faster
+      // (FP8: polling -3 %).
+      auto wait_p = [&](uint64_t* bar, int u) {
+        return (!FP8 && D == 128) ? mbar_wait_poll(bar, u & 1, &sh.abort, &g_err_fwd)
+                                  : mbar_wait<true>(bar, u & 1, &sh.abort, &g_err_fwd);
       };
       auto wait_load = [&](int idx) {
         return mbar_wait<true>(&sh.kv_full[idx % C::kSlots], (idx / C::kSlots) & 1, &sh.abort, &g_err_fwd);
@@ -350,14 +367,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = wait_load(v_idx);
               v_ready = true;
             }
-            // bf16 at d = 128 polls for P (+0.3 % causal, +1.7 % without a mask,
-            // measured); elsewhere the suspending wait measured as fast or faster
-            // (FP8: polling -3 %).
-            ok = ok && ((!FP8 && D == 128) ? mbar_wait_poll(&sh.p_full[t], u & 1, &sh.abort, &g_err_fwd)
-                                           : mbar_wait<true>(&sh.p_full[t], u & 1, &sh.abort, &g_err_fwd));
+            if constexpr (C::kSplitP) {  // keys 0-63 as soon as their P is there
+              ok = ok && wait_p(&sh.p_half[t], u);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, v_idx % C::kSlots, u > 0, 0, C::kPVSteps / 2);
+            }
+            ok = ok && wait_p(&sh.p_full[t], u);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(t, v_idx % C::kSlots, u > 0);
+            issue_pv(t, v_idx % C::kSlots, u > 0, C::kSplitP ? C::kPVSteps / 2 : 0, C::kPVSteps);
+            tc_commit(&sh.o_done[t]);
           }
           // ... and right behind it S_t(u+1) into the same columns.
           if (u + 1 >= 0 && u + 1 < len[t]) {
@@ -494,6 +514,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_ref = ((WIN && m_used == -INFINITY) ? 0.0f : m_used) + C::kPShiftLog2;
       // P over S_t: the first half's words go to the first columns (all of
       // S_t is in registers by now).
+      // O_t may be rescaled once S_t(u) has completed (PV_t(u-1), issued before
+      // it, is complete too), and must be before any PV_t(u): with P handed
+      // over in halves, after the first half's P (when half of S is no longer
+      // held in registers), else after both.
+      auto rescale_o = [&]() {
+        if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t rr[32];
+            tmem_ld32(o_col + cc, rr);
+            tmem_ld_wait(rr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(o_col + cc, rr);
+          }
+        }
+      };
       float row_sum;
       {
         uint32_t pw[C::kPWordsHalf];
@@ -501,26 +538,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (FP8) tmem_st16(s_col, pw);
         else tmem_st32(s_col, pw);
       }
+      if constexpr (C::kSplitP) {  // keys 0-63 handed over
+        rescale_o();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sh.p_half[t]);
+      }
       {
         uint32_t pw[C::kPWordsHalf];
         row_sum += exp2_pack_row<FP8, C::kEmuGroups, C::kPolyDeg, BS>(s1, c1, m_ref, pw, pm1);
         if constexpr (FP8) tmem_st16(s_col + 16, pw);
         else tmem_st32(s_col + 32, pw);
       }
-      // O_t may be rescaled now: S_t(u) completing means PV_t(u-1), issued
-      // before it, is complete too (done after P, when S is no longer held
-      // in registers).
-      if (__any_sync(0xffffffffu, raise)) {
-#pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t rr[32];
-          tmem_ld32(o_col + cc, rr);
-          tmem_ld_wait(rr);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-          tmem_st32(o_col + cc, rr);
-        }
-      }
+      if constexpr (!C::kSplitP) rescale_o();  // (after both halves: no S left in registers)
       l_sum = l_sum * alpha + row_sum;
       tmem_st_wait();
       tc_fence_before();
