@@ -99,7 +99,9 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __r
   pdl_launch_dependents();
   pdl_wait_prior();
   // Groups of 8 values; each thread keeps four groups' loads in flight before
-  // converting and storing them.
+  // converting and storing them.  Both streams are touched once: loads and
+  // stores marked evict-first (measured: 35.3 -> 32.8 us on the long causal
+  // workload's 134 MB accumulator).
   constexpr int kU = 4;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -107,8 +109,8 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __r
     float4 a[kU], b[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      a[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * (i + u * stride));
-      b[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * (i + u * stride) + 1);
+      a[u] = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * (i + u * stride));
+      b[u] = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * (i + u * stride) + 1);
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
@@ -117,7 +119,7 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert_kernel(const float* __r
       r.y = pack_bf16x2(a[u].z * scale, a[u].w * scale);
       r.z = pack_bf16x2(b[u].x * scale, b[u].y * scale);
       r.w = pack_bf16x2(b[u].z * scale, b[u].w * scale);
-      reinterpret_cast<uint4*>(dq)[i + u * stride] = r;
+      __stcs(reinterpret_cast<uint4*>(dq) + i + u * stride, r);
     }
   }
   for (; i < n8; i += stride) {
