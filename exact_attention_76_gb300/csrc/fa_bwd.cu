@@ -221,9 +221,9 @@ template <int D, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
-                       const __grid_constant__ CUtensorMap map_dq, const float* __restrict__ lse,
-                       const float* __restrict__ dvec, __nv_bfloat16* __restrict__ dk_out,
-                       __nv_bfloat16* __restrict__ dv_out, int BH, int N, int causal, float scale,
+                       const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_dk,
+                       const __grid_constant__ CUtensorMap map_dv, const float* __restrict__ lse,
+                       const float* __restrict__ dvec, int BH, int N, int causal, float scale,
                        float scale_log2, int head_group, int H, int qgroup, int window) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -234,9 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicOr(&g_err_bwd, 2u);
     return;
   }
-  // A wait of an earlier CTA ran out: the launch is already failed, stop here
-  // (the word stays set until fa_device_error reads and clears it).
-  if (*reinterpret_cast<volatile uint32_t*>(&g_err_bwd) & FA_DEVERR_TIMEOUT) return;
+
   float* s_lse2 = reinterpret_cast<float*>(smem + C::kOffL);
   float* s_dvec = reinterpret_cast<float*>(smem + C::kOffDv);
 
@@ -268,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (threadIdx.x == 0) {
-    sh.abort.flag = 0;
+    // A wait of an earlier CTA ran out: the launch is already failed, and this
+    // CTA stops after its set-up (the word stays set until fa_device_error
+    // reads and clears it).  The load's latency overlaps the set-up.
+    const uint32_t err0 = *reinterpret_cast<volatile uint32_t*>(&g_err_bwd);
     mbar_init(&sh.kv_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sh.q_full[s], 1);
@@ -287,12 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.acc_done, 1);
     mbar_init(&sh.drain, 1);
     fence_barrier_init();
+    sh.abort.flag = (err0 & FA_DEVERR_TIMEOUT) ? 1 : 0;
   }
   if (warp == 9) tmem_alloc(&sh.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+  if (sh.abort.flag) {
+    if (warp == 9) tmem_dealloc(tmem, 512);
+    return;
+  }
   // Set-up done: the next kernel may start launching; inputs are read only
   // after the kernels before this one have completed.
   pdl_launch_dependents();
@@ -496,7 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = half * 64;  // first query of this warpgroup's half
     const int r = static_cast<int>((warp & 3) * 32 + lane_id());  // key row within the block == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int kg = kb * 128 + r;
     uint8_t* ds_row = smem + C::kOffDS + half * C::kBlockBytes + r * 128;
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     bool ok = true;
@@ -597,23 +602,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sh.ds_ready);
       mbar_arrive(&sh.ld_empty[st]);
     }
-    // dV = sum_i P_i^T dO_i, each warpgroup writing half of the columns
-    if (ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd)) {
-      tc_fence_after();
-      const bool store = kg < N;
-      __nv_bfloat16* dst = dv_out + (static_cast<size_t>(bh) * N + (store ? kg : 0)) * D;
-#pragma unroll 1
-      for (int cc = half * (D / 2); cc < (half + 1) * (D / 2); cc += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kTmDV + cc, rr);
-        tmem_ld_wait(rr);
-        uint32_t pk[16];
+    // dV = sum_i P_i^T dO_i, each warpgroup writing half of the columns, staged
+    // with the 128-byte swizzle in K's dead space (every product has completed
+    // once acc_done has) and written by TMA stores, which drop rows past N
+    // (measured against per-thread row stores: +4 % on the backward at N = 512
+    // and 1024, d = 128).  At d = 128 each warpgroup's 64 columns are a box of
+    // their own; at d = 64 the two halves share one box.
+    {
+      constexpr int kCols = D / 2;
+      bool ok2 = ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd);
+      if (ok2) {
+        tc_fence_after();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
-        if (store) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+        for (int cc = 0; cc < kCols; cc += 32) {
+          const int col = half * kCols + cc;
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + C::kTmDV + col, rr);
+          tmem_ld_wait(rr);
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]), __uint_as_float(rr[2 * i + 1]));
+          uint8_t* box = smem + C::kOffK + (col / 64) * C::kBlockBytes;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(box + r * 128 + ((static_cast<uint32_t>((col % 64) / 8 + i) ^ swz) << 4)) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+        fence_proxy_async_smem();
+      }
+      if constexpr (D == 128) {
+        ok2 = named_bar_and(2 + half, 128, ok2);
+        if (ok2 && (warp & 3) == 0 && lane_id() == 0) {
+          tma_store_3d(&map_dv, half * 64, kb * 128, bh, smem + C::kOffK + half * C::kBlockBytes);
+          bulk_commit_group();
+          bulk_wait_read_all();
+        }
+      } else {
+        ok2 = named_bar_and(2, 256, ok2);
+        if (ok2 && threadIdx.x == 0) {
+          tma_store_3d(&map_dv, 0, kb * 128, bh, smem + C::kOffK);
+          bulk_commit_group();
+          bulk_wait_read_all();
         }
       }
     }
@@ -673,27 +702,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       staged_before = true;
     }
-    if (leader) bulk_wait_all();
-    // dK = scale * sum_i dS_i^T Q_i
-    if (ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd)) {
-      tc_fence_after();
-      const int kg = kb * 128 + r;
-      const bool store = kg < N;
-      __nv_bfloat16* dst = dk_out + (static_cast<size_t>(bh) * N + (store ? kg : 0)) * D;
-#pragma unroll 1
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::kTmDK + cc, rr);
-        tmem_ld_wait(rr);
-        uint32_t pk[16];
+    if (leader) bulk_wait_read_all();
+    // dK = scale * sum_i dS_i^T Q_i, staged in V's dead space (D / 64 boxes of
+    // 64 columns) and written by TMA stores.
+    {
+      bool ok2 = ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd);
+      if (ok2) {
+        tc_fence_after();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * scale, __uint_as_float(rr[2 * i + 1]) * scale);
-        if (store) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + C::kTmDK + cc, rr);
+          tmem_ld_wait(rr);
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * scale, __uint_as_float(rr[2 * i + 1]) * scale);
+          uint8_t* box = smem + C::kOffV + (cc / 64) * C::kBlockBytes;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(box + r * 128 + ((static_cast<uint32_t>((cc % 64) / 8 + i) ^ swz) << 4)) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
+        fence_proxy_async_smem();
+      }
+      ok2 = named_bar_and(1, 128, ok2);
+      if (ok2 && leader) {
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b)
+          tma_store_3d(&map_dk, b * 64, kb * 128, bh, smem + C::kOffV + b * C::kBlockBytes);
+        bulk_commit_group();
+        bulk_wait_read_all();
       }
     }
   }
@@ -712,10 +751,11 @@ fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   const int BHq = a.B * a.H;     // query heads
   const int BH = a.B * a.Hkv;    // key/value heads: one CTA column each
   const int qgroup = a.H / a.Hkv;
-  CUtensorMap mq, mk, mv, mdo, mdq;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if (!encode_rows_map(&mq, a.q, 2, D, a.N, BHq, 64, 128) || !encode_rows_map(&mk, a.k, 2, D, a.N, BH, 64, 128) ||
       !encode_rows_map(&mv, a.v, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdo, a.dO, 2, D, a.N, BHq, 64, 128) ||
-      !encode_rows_map(&mdq, a.dq_acc, 4, D, a.N, BHq, 32, 128))
+      !encode_rows_map(&mdq, a.dq_acc, 4, D, a.N, BHq, 32, 128) ||
+      !encode_rows_map(&mdk, a.dk, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdv, a.dv, 2, D, a.N, BH, 64, 128))
     return FA_ERR_LAUNCH;
   auto kern = fa_bwd_main_kernel<D, WIN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
@@ -734,9 +774,9 @@ fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   int group = static_cast<int>(std::max<long long>(1, (48ll << 20) / head_bytes));
   group = std::min(group, BH);
   dim3 grid(static_cast<unsigned>(n_blk * BH));
-  const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), C::kSmemBytes, stream, mq, mk, mv, mdo, mdq, a.lse,
-                                   a.D, static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), BH, a.N,
-                                   a.causal, a.scale, a.scale * kLog2e, group, a.H, qgroup, a.window);
+  const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), C::kSmemBytes, stream, mq, mk, mv, mdo, mdq, mdk, mdv,
+                                   a.lse, a.D, BH, a.N, a.causal, a.scale, a.scale * kLog2e, group, a.H, qgroup,
+                                   a.window);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -222,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* s_q = smem;                       // two Q tiles
   uint8_t* s_kv = smem + 2 * C::kTileBytes;  // ring of K/V slots
 
-  if (*reinterpret_cast<volatile uint32_t*>(&g_err_fwd) & FA_DEVERR_TIMEOUT) return;
   const int warp = warp_id();
   const int n_qblk = (N + 2 * kBM - 1) / (2 * kBM);
   int bh, qb;
@@ -248,7 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_max = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
-    sh.abort.flag = 0;
+    // A wait of an earlier CTA ran out: this CTA stops after its set-up; the
+    // load's latency overlaps the set-up.
+    const uint32_t err0 = *reinterpret_cast<volatile uint32_t*>(&g_err_fwd);
     mbar_init(&sh.q_full, 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(&sh.kv_full[s], 1);
@@ -262,12 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sh.drain, 1);
     fence_barrier_init();
+    sh.abort.flag = (err0 & FA_DEVERR_TIMEOUT) ? 1 : 0;
   }
   if (warp == 9) tmem_alloc(&sh.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+  if (sh.abort.flag) {
+    if (warp == 9) tmem_dealloc(tmem, 512);
+    return;
+  }
   // Set-up done: the next kernel may start launching; inputs are read only
   // after the kernels before this one have completed.
   pdl_launch_dependents();
