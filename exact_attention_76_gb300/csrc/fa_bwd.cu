@@ -55,6 +55,9 @@ constexpr int kThreads = 512;
 // setmaxnreg split below must add up to the launch allocation.
 constexpr int kRegLaunch = 128;
 constexpr float kLog2e = 1.4426950408889634f;
+// Rows (B * H * N) up to which the preprocess and convert kernels are launched
+// with programmatic stream serialization (see launch_bwd_preprocess).
+constexpr long long kSmallRows = 65536;
 
 // ---------------------------------------------------------------- preprocess
 
@@ -787,15 +790,24 @@ fa_status launch_bwd_preprocess(const void* o, const void* dO, float* D, float* 
   const int rows_per_block = 256 / (d / 8);
   const long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  // A plain launch: launched early, its many small CTAs would sit beside the
-  // previous kernel's last CTAs and slow them (measured: +3 % on the long
-  // causal step); it still lets the backward main kernel launch early.
+  // A plain launch except for small problems: launched early, its many small
+  // CTAs sit beside the previous kernel's last CTAs and slow them (measured:
+  // +4 % on the long causal step, +2 % at N = 512 and 1024 with B*H = 512 and
+  // 256), while at B*H*N <= 65536 rows the overlap wins (it and the convert
+  // launched early: the GPT-2-small-like fwd+bwd step 70.5 -> 65.5 us).  Either
+  // way the backward main kernel may launch early behind it.
   const auto* o16 = static_cast<const __nv_bfloat16*>(o);
   const auto* do16 = static_cast<const __nv_bfloat16*>(dO);
   const dim3 grid(static_cast<unsigned>(blocks));
-  if (d == 64) fa_bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(o16, do16, D, dq_acc, rows);
-  else fa_bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(o16, do16, D, dq_acc, rows);
-  const cudaError_t e = cudaPeekAtLastError();
+  cudaError_t e;
+  if (rows <= kSmallRows) {
+    e = d == 64 ? launch_pdl(fa_bwd_preprocess_kernel<64>, grid, dim3(256), 0, stream, o16, do16, D, dq_acc, rows)
+                : launch_pdl(fa_bwd_preprocess_kernel<128>, grid, dim3(256), 0, stream, o16, do16, D, dq_acc, rows);
+  } else {
+    if (d == 64) fa_bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(o16, do16, D, dq_acc, rows);
+    else fa_bwd_preprocess_kernel<128><<<grid, 256, 0, stream>>>(o16, do16, D, dq_acc, rows);
+    e = cudaPeekAtLastError();
+  }
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -815,10 +827,16 @@ fa_status launch_bwd_dq_convert(const float* dq_acc, void* dq, long long rows, i
   const long long cap = static_cast<long long>(sms) * 8;  // grid-stride beyond 8 waves of 256 threads
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  // A plain launch, as for the preprocess kernel.
-  fa_bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
-                                                                               n8, scale);
-  const cudaError_t e = cudaPeekAtLastError();
+  // Launched as the preprocess kernel is: early only for small problems.
+  cudaError_t e;
+  if (rows <= kSmallRows) {
+    e = launch_pdl(fa_bwd_dq_convert_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, dq_acc,
+                   static_cast<__nv_bfloat16*>(dq), n8, scale);
+  } else {
+    fa_bwd_dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(dq_acc,
+                                                                                 static_cast<__nv_bfloat16*>(dq), n8, scale);
+    e = cudaPeekAtLastError();
+  }
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
