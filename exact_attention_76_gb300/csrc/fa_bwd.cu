@@ -31,7 +31,14 @@
 //  warps 4-7  thread r owns query row r of the current block: reads dQ_i
 //             from TMEM and adds it into the fp32 accumulator; finally
 //             writes dK = scale * acc.
-//  warp 8     TMA producer: K and V once, Q_i into two stages, dO_i into one.
+//  warp 8     TMA producer: K and V once, Q_i into two stages, dO_i into one
+//             (d = 64: three and two).
+//
+// Per query block the MMA thread issues, at d = 128, dV_i, S_(i+1), dK_i,
+// dQ_i, dP_(i+1) (dQ_i shares dP^T's TMEM columns); at d = 64, where S^T, P^T,
+// dP^T and dQ each have columns of their own, S_(i+1) as soon as the key rows
+// have read S_i, then dV_i, dP_(i+1) as soon as they have read dP_i, then dK_i
+// and dQ_i, so that both are ready before the key rows need them.
 //  warp 9     TMEM allocation and the single MMA-issuing thread.
 //  warp 10    L_i and D_i of each query block into shared memory (two stages).
 //  warp 11    no role (it completes the TMA/MMA warpgroup).
@@ -149,9 +156,18 @@ struct BwdCfg {
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ = kOffV + kTileBytes;           // 2 stages
-  static constexpr int kOffDO = kOffQ + 2 * kTileBytes;      // 1 stage
-  static constexpr int kOffDS = kOffDO + kTileBytes;
+  // At d = 64 the next block's S^T and dP^T are issued as soon as the key rows
+  // have read this block's (their TMEM columns are not shared with P or dQ
+  // there), and shared memory has room for the copies that feeds: three Q and
+  // two dO stages (measured: +6-7 % on the d = 64 backward at N = 8192 and
+  // 16384, +1-4 % at N = 512 and 1024).  A second dS^T buffer or dV issued
+  // before the next S measured the same or slower.
+  static constexpr bool kEarly = (D == 64);
+  static constexpr int kQStages = kEarly ? 3 : 2;
+  static constexpr int kDoStages = kEarly ? 2 : 1;
+  static constexpr int kOffQ = kOffV + kTileBytes;                  // kQStages stages
+  static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;      // kDoStages stages
+  static constexpr int kOffDS = kOffDO + kDoStages * kTileBytes;
   static constexpr int kOffStage = kOffDS + kDsBytes;
   static constexpr int kOffL = kOffStage + kStageBytes;      // float [2][128]
   static constexpr int kOffDv = kOffL + 2 * 128 * 4;         // float [2][128]
@@ -186,9 +202,10 @@ struct BwdCfg {
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t q_full[2];
-  uint64_t q_empty[2];
-  uint64_t do_full, do_empty;
+  uint64_t q_full[3];
+  uint64_t q_empty[3];
+  uint64_t do_full[2], do_empty[2];
+  uint64_t s_free, dp_free;
   uint64_t ld_full[2];
   uint64_t ld_empty[2];
   uint64_t s_full, p_ready, dp_full, ds_ready, dq_full, dq_free, acc_done, drain;
@@ -274,14 +291,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // reads and clears it).  The load's latency overlaps the set-up.
     const uint32_t err0 = *reinterpret_cast<volatile uint32_t*>(&g_err_bwd);
     mbar_init(&sh.kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&sh.q_full[s], 1);
       mbar_init(&sh.q_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&sh.ld_full[s], 32);
       mbar_init(&sh.ld_empty[s], 256);
     }
-    mbar_init(&sh.do_full, 1);
-    mbar_init(&sh.do_empty, 1);
+    for (int s = 0; s < C::kDoStages; ++s) {
+      mbar_init(&sh.do_full[s], 1);
+      mbar_init(&sh.do_empty[s], 1);
+    }
+    mbar_init(&sh.s_free, 256);
+    mbar_init(&sh.dp_free, 256);
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.p_ready, 256);
     mbar_init(&sh.dp_full, 1);
@@ -323,19 +346,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + C::kOffV + cb * C::kBlockBytes, &map_v, cb * 64, kb * 128, bh, &sh.kv_full);
         }
       }
-      int q_issued[2] = {0, 0};
-      int do_issued = 0;
+      int q_issued[C::kQStages] = {};
+      int do_issued[C::kDoStages] = {};
       QCursor cur{i_begin, qh0};
       for (int it = 0; it < n_it; ++it) {
         q_advance(cur, it);
         if (__shfl_sync(0xffffffffu, sh.abort.flag, 0)) break;  // one decision for the whole warp
-        const int st = it & 1;
-        const int use = it >> 1;
+        const int st = it % C::kQStages;
+        const int use = it / C::kQStages;
+        const int sd = it % C::kDoStages;
+        const int used = it / C::kDoStages;
         const int qrow0 = cur.i * 128;
         const int qh = cur.h;
         bool ok = true;
         if (lane == 0) {
-          // Q_i: two stages, freed when dK_(i-2) has read it.
+          // Q_i: kQStages stages, each freed when the dK that read it is done.
           if (use > 0) ok = mbar_wait(&sh.q_empty[st], (use - 1) & 1, &sh.abort, &g_err_bwd);
           if (ok) {
             mbar_arrive_expect_tx(&sh.q_full[st], C::kTileBytes);
@@ -344,13 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                           &sh.q_full[st]);
             ++q_issued[st];
           }
-          // dO_i: one stage, freed when dV_(i-1) has read it.
-          if (ok && it > 0) ok = mbar_wait(&sh.do_empty, (it - 1) & 1, &sh.abort, &g_err_bwd);
+          // dO_i: kDoStages stages, each freed when the dV that read it is done.
+          if (ok && used > 0) ok = mbar_wait(&sh.do_empty[sd], (used - 1) & 1, &sh.abort, &g_err_bwd);
           if (ok) {
-            mbar_arrive_expect_tx(&sh.do_full, C::kTileBytes);
+            mbar_arrive_expect_tx(&sh.do_full[sd], C::kTileBytes);
             for (int cb = 0; cb < C::kColBlocks; ++cb)
-              tma_load_3d(smem + C::kOffDO + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, qh, &sh.do_full);
-            ++do_issued;
+              tma_load_3d(smem + C::kOffDO + sd * C::kTileBytes + cb * C::kBlockBytes, &map_do, cb * 64, qrow0, qh,
+                          &sh.do_full[sd]);
+            ++do_issued[sd];
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -359,9 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && sh.abort.flag) {
         // Let every copy still in flight land before the CTA's memory goes away.
         mbar_wait_drain(&sh.kv_full, 0, &g_err_bwd);
-        for (int s2 = 0; s2 < 2; ++s2)
+        for (int s2 = 0; s2 < C::kQStages; ++s2)
           if (q_issued[s2] > 0) mbar_wait_drain(&sh.q_full[s2], (q_issued[s2] - 1) & 1, &g_err_bwd);
-        if (do_issued > 0) mbar_wait_drain(&sh.do_full, (do_issued - 1) & 1, &g_err_bwd);
+        for (int s2 = 0; s2 < C::kDoStages; ++s2)
+          if (do_issued[s2] > 0) mbar_wait_drain(&sh.do_full[s2], (do_issued[s2] - 1) & 1, &g_err_bwd);
       }
       __syncwarp();
     } else if (warp == 9) {
@@ -379,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t do_k = sdesc_sw128(sm + C::kOffDO, 16, 1024), do_mn = sdesc_sw128(sm + C::kOffDO, C::kBlockBytes, 1024);
         const uint64_t q_k = sdesc_sw128(sm + C::kOffQ, 16, 1024), q_mn = sdesc_sw128(sm + C::kOffQ, C::kBlockBytes, 1024);
         auto issue_s = [&](int i) {  // S^T = K Q_i^T
-          const uint64_t qb = sdesc_advance(q_k, (i & 1) * C::kTileBytes);
+          const uint64_t qb = sdesc_advance(q_k, (i % C::kQStages) * C::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
@@ -387,11 +414,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(&sh.s_full);
         };
-        auto issue_dp = [&]() {  // dP^T = V dO_i^T
+        auto issue_dp = [&](int i) {  // dP^T = V dO_i^T
+          const uint64_t db = sdesc_advance(do_k, (i % C::kDoStages) * C::kTileBytes);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
-            mma_bf16_ss(tmem + C::kTmDP, sdesc_advance(v_k, off), sdesc_advance(do_k, off), C::kIdescKK, kk > 0);
+            mma_bf16_ss(tmem + C::kTmDP, sdesc_advance(v_k, off), sdesc_advance(db, off), C::kIdescKK, kk > 0);
           }
           tc_commit(&sh.dp_full);
         };
@@ -400,16 +428,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           tc_fence_after();
           issue_s(0);
-          ok = mbar_wait(&sh.do_full, 0, &sh.abort, &g_err_bwd);
+          ok = mbar_wait(&sh.do_full[0], 0, &sh.abort, &g_err_bwd);
           if (ok) {
             tc_fence_after();
-            issue_dp();
+            issue_dp(0);
           }
         }
         for (int it = 0; ok && it < n_it; ++it) {
-          const int st = it & 1;
+          const int st = it % C::kQStages;
           const uint64_t qm = sdesc_advance(q_mn, st * C::kTileBytes);
+          const uint64_t dom = sdesc_advance(do_mn, (it % C::kDoStages) * C::kTileBytes);
           const bool has_next = it + 1 < n_it;
+          if constexpr (C::kEarly) {
+            // S_(i+1) once the key rows have read S_i ...
+            if (has_next) {
+              ok = mbar_wait(&sh.s_free, it & 1, &sh.abort, &g_err_bwd) &&
+                   mbar_wait(&sh.q_full[(it + 1) % C::kQStages], ((it + 1) / C::kQStages) & 1, &sh.abort, &g_err_bwd);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(it + 1);
+            }
+            // ... dV_i once they wrote P_i ...
+            ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmP + kk * 8, sdesc_advance(dom, kk * 2048), C::kIdescKM,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&sh.do_empty[it % C::kDoStages]);
+            // ... dP_(i+1) once they have read dP_i ...
+            if (has_next) {
+              ok = mbar_wait(&sh.dp_free, it & 1, &sh.abort, &g_err_bwd) &&
+                   mbar_wait(&sh.do_full[(it + 1) % C::kDoStages], ((it + 1) / C::kDoStages) & 1, &sh.abort,
+                             &g_err_bwd);
+              if (!ok) break;
+              tc_fence_after();
+              issue_dp(it + 1);
+            }
+            // ... and dK_i, dQ_i once they wrote dS_i (dQ_i after the read-out of dQ_(i-1)).
+            ok = mbar_wait(&sh.ds_ready, it & 1, &sh.abort, &g_err_bwd);
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kBlockBytes + (kk & 3) * 32;
+              mma_bf16_ss(tmem + C::kTmDK, sdesc_advance(ds_k, off), sdesc_advance(qm, kk * 2048), C::kIdescKM,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(&sh.q_empty[st]);
+            if (it > 0) {
+              ok = mbar_wait(&sh.dq_free, (it - 1) & 1, &sh.abort, &g_err_bwd);
+              if (!ok) break;
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ss(tmem + C::kTmDQ, sdesc_advance(ds_mn, kk * 2048), sdesc_advance(k_mn, kk * 2048), C::kIdescMM,
+                          kk > 0);
+            tc_commit(&sh.dq_full);
+            continue;
+          }
           // dV += P_i^T dO_i
           ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
           if (!ok) break;
@@ -417,14 +496,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmP + kk * 8 + ((C::kOwnP || kk < 4) ? 0 : 64),
-                        sdesc_advance(do_mn, kk * 2048), C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(&sh.do_empty);
+                        sdesc_advance(dom, kk * 2048), C::kIdescKM, (it > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&sh.do_empty[it % C::kDoStages]);
           // S_(i+1): at d = 128 its columns hold P_i^T, which dV_i reads.  The
           // tcgen05.mma operations of one thread execute in issue order, so
           // S_(i+1) issued right behind dV_i overwrites P_i^T only after dV_i
           // has read it (measured: +0.5 % over waiting for dV_i to complete).
           if (has_next) {
-            ok = mbar_wait(&sh.q_full[(it + 1) & 1], ((it + 1) >> 1) & 1, &sh.abort, &g_err_bwd);
+            ok = mbar_wait(&sh.q_full[(it + 1) % C::kQStages], ((it + 1) / C::kQStages) & 1, &sh.abort, &g_err_bwd);
             if (!ok) break;
             tc_fence_after();
             issue_s(it + 1);
@@ -452,12 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(&sh.dq_full);
           // dP_(i+1)
           if (has_next) {
-            ok = mbar_wait(&sh.do_full, (it + 1) & 1, &sh.abort, &g_err_bwd);
+            ok = mbar_wait(&sh.do_full[(it + 1) % C::kDoStages], ((it + 1) / C::kDoStages) & 1, &sh.abort, &g_err_bwd);
             if (ok && D == 128)  // dP^T shares columns with dQ_i
               ok = mbar_wait(&sh.dq_free, it & 1, &sh.abort, &g_err_bwd);
             if (!ok) break;
             tc_fence_after();
-            issue_dp();
+            issue_dp(it + 1);
           }
         }
         if (ok) tc_commit(&sh.acc_done);
@@ -550,6 +629,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + C::kTmS + c0 + 32, rs[1]);
         tmem_ld_wait(rs[0]);
         tmem_ld_wait(rs[1]);
+        if constexpr (C::kEarly) {  // S^T's columns may take S_(i+1)
+          tc_fence_before();
+          mbar_arrive(&sh.s_free);
+        }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
@@ -578,6 +661,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rr[32];
         tmem_ld32(tmem + lane_base + C::kTmDP + c0 + cc * 32, rr);
         tmem_ld_wait(rr);
+        if constexpr (C::kEarly) {
+          if (cc == 1) {  // dP^T's columns may take dP_(i+1)
+            tc_fence_before();
+            mbar_arrive(&sh.dp_free);
+          }
+        }
         // 32 queries = four 16-byte chunks of 8 in this half's column block
         uint32_t w[16];
 #pragma unroll
