@@ -36,9 +36,9 @@
 //
 // Per query block the MMA thread issues, at d = 128, dV_i, S_(i+1), dK_i,
 // dQ_i, dP_(i+1) (dQ_i shares dP^T's TMEM columns); at d = 64, where S^T, P^T,
-// dP^T and dQ each have columns of their own, S_(i+1) as soon as the key rows
-// have read S_i, then dV_i, dP_(i+1) as soon as they have read dP_i, then dK_i
-// and dQ_i, so that both are ready before the key rows need them.
+// dP^T and dQ each have columns of their own, dV_i and S_(i+1), then
+// dP_(i+1) as soon as the key rows have read dP_i, then dK_i and dQ_i, so that
+// the next S and dP are ready before the key rows need them.
 //  warp 9     TMEM allocation and the single MMA-issuing thread.
 //  warp 10    L_i and D_i of each query block into shared memory (two stages).
 //  warp 11    no role (it completes the TMA/MMA warpgroup).
@@ -156,12 +156,12 @@ struct BwdCfg {
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kTileBytes;
-  // At d = 64 the next block's S^T and dP^T are issued as soon as the key rows
-  // have read this block's (their TMEM columns are not shared with P or dQ
-  // there), and shared memory has room for the copies that feeds: three Q and
-  // two dO stages (measured: +6-7 % on the d = 64 backward at N = 8192 and
-  // 16384, +1-4 % at N = 512 and 1024).  A second dS^T buffer or dV issued
-  // before the next S measured the same or slower.
+  // At d = 64 the next block's dP^T is issued as soon as the key rows have read
+  // this block's, and the next S^T right behind dV (their TMEM columns are not
+  // shared with P or dQ there); shared memory has room for the copies that
+  // feeds: three Q and two dO stages (measured: +6-7 % on the d = 64 backward
+  // at N = 8192 and 16384, +1-4 % at N = 512 and 1024).  A second dS^T buffer
+  // measured the same or slower.
   static constexpr bool kEarly = (D == 64);
   static constexpr int kQStages = kEarly ? 3 : 2;
   static constexpr int kDoStages = kEarly ? 2 : 1;
@@ -200,17 +200,18 @@ struct BwdCfg {
   static_assert(2 * kRegKeyRow + kRegCtl + kRegDq == 4 * kRegLaunch, "register split");
 };
 
+template <int D>
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t q_full[3];
-  uint64_t q_empty[3];
-  uint64_t do_full[2], do_empty[2];
-  uint64_t s_free, dp_free;
+  uint64_t q_full[BwdCfg<D>::kQStages];
+  uint64_t q_empty[BwdCfg<D>::kQStages];
+  uint64_t do_full[BwdCfg<D>::kDoStages], do_empty[BwdCfg<D>::kDoStages];
   uint64_t ld_full[2];
   uint64_t ld_empty[2];
   uint64_t s_full, p_ready, dp_full, ds_ready, dq_full, dq_free, acc_done, drain;
   uint32_t tmem_base;
   CtaAbort abort;
+  uint64_t dp_free;  // d = 64 only
 };
 
 // Block index -> (head, key block).  Heads are taken in groups whose Q, dO
@@ -247,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        float scale_log2, int head_group, int H, int qgroup, int window) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  static_assert(sizeof(BwdBars) <= 256, "barrier block");
-  BwdBars& sh = *reinterpret_cast<BwdBars*>(smem + C::kOffBar);
+  static_assert(sizeof(BwdBars<D>) <= 256, "barrier block");
+  BwdBars<D>& sh = *reinterpret_cast<BwdBars<D>*>(smem + C::kOffBar);
   // The tile offsets assume a 1024-byte aligned base (the swizzle atoms).
   if ((smem_u32(smem) & 1023u) != 0) {
     if (threadIdx.x == 0) atomicOr(&g_err_bwd, 2u);
@@ -303,7 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.do_full[s], 1);
       mbar_init(&sh.do_empty[s], 1);
     }
-    mbar_init(&sh.s_free, 256);
     mbar_init(&sh.dp_free, 256);
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.p_ready, 256);
@@ -440,15 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t dom = sdesc_advance(do_mn, (it % C::kDoStages) * C::kTileBytes);
           const bool has_next = it + 1 < n_it;
           if constexpr (C::kEarly) {
-            // S_(i+1) once the key rows have read S_i ...
-            if (has_next) {
-              ok = mbar_wait(&sh.s_free, it & 1, &sh.abort, &g_err_bwd) &&
-                   mbar_wait(&sh.q_full[(it + 1) % C::kQStages], ((it + 1) / C::kQStages) & 1, &sh.abort, &g_err_bwd);
-              if (!ok) break;
-              tc_fence_after();
-              issue_s(it + 1);
-            }
-            // ... dV_i once they wrote P_i ...
+            // dV_i once the key rows wrote P_i ...
             ok = mbar_wait(&sh.p_ready, it & 1, &sh.abort, &g_err_bwd);
             if (!ok) break;
             tc_fence_after();
@@ -457,6 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_ts(tmem + C::kTmDV, tmem + C::kTmP + kk * 8, sdesc_advance(dom, kk * 2048), C::kIdescKM,
                           (it > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&sh.do_empty[it % C::kDoStages]);
+            // ... S_(i+1) right behind it (the key rows read S_i before writing
+            // P_i; issued after dV_i, its completion, which they await before
+            // writing P_(i+1), covers dV_i's reads of P_i) ...
+            if (has_next) {
+              ok = mbar_wait(&sh.q_full[(it + 1) % C::kQStages], ((it + 1) / C::kQStages) & 1, &sh.abort, &g_err_bwd);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(it + 1);
+            }
             // ... dP_(i+1) once they have read dP_i ...
             if (has_next) {
               ok = mbar_wait(&sh.dp_free, it & 1, &sh.abort, &g_err_bwd) &&
@@ -629,10 +630,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_base + C::kTmS + c0 + 32, rs[1]);
         tmem_ld_wait(rs[0]);
         tmem_ld_wait(rs[1]);
-        if constexpr (C::kEarly) {  // S^T's columns may take S_(i+1)
-          tc_fence_before();
-          mbar_arrive(&sh.s_free);
-        }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
