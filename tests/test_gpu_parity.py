@@ -444,6 +444,8 @@ WINDOW_CASES = [
     (1, 4, 2, 1000, 128, 100),  # grouped queries, ragged tail
     (1, 2, 2, 1000, 128, 257),  # window spans tiles; the second tile starts later
     (2, 2, 1, 777, 64, 700),
+    (1, 2, 2, 1000, 64, 257),   # d = 64: the second tile starts later, S issued ahead of the softmax
+    (1, 4, 2, 2000, 64, 300),
 ]
 
 
