@@ -18,7 +18,8 @@
 //       dP^T = V dO_i^T       (smem x smem)        -> TMEM
 //       dV  += P^T dO_i       (P^T from TMEM)      -> TMEM, whole loop
 //       dK  += dS^T Q_i       (dS^T from smem)     -> TMEM, whole loop
-//       dQ_i = dS K           (dS^T read MN-major) -> TMEM, then fp32 atomics
+//       dQ_i = dS K           (dS^T read MN-major) -> TMEM, then TMA reduce-adds
+//                                                     into an fp32 accumulator
 //     Causal: query blocks below the key block are skipped; only the
 //     diagonal block applies the element mask.
 //  3. fa_bwd_dq_convert: dQ = bf16(scale * dQ_acc).  HBM bound.
@@ -26,22 +27,22 @@
 // Roles of fa_bwd_main_kernel (512 threads, four warpgroups):
 //  warps 0-3  thread r owns key row r for queries 0-63 of the block:
 //             P^T = exp2(S^T c - L_i log2 e) into TMEM (bf16; over S^T at d = 128), then
-//             dS^T = P^T o (dP^T - D_i) into smem; finally half of dV.
+//             dS^T = P^T o (dP^T - D_i) into smem; finally half of dV (TMA store).
 //  warps 12-15 the same for queries 64-127 and the other half of dV.
 //  warps 4-7  thread r owns query row r of the current block: reads dQ_i
 //             from TMEM and adds it into the fp32 accumulator; finally
-//             writes dK = scale * acc.
+//             writes dK = scale * acc (TMA store).
 //  warp 8     TMA producer: K and V once, Q_i into two stages, dO_i into one
 //             (d = 64: three and two).
+//  warp 9     TMEM allocation and the single MMA-issuing thread.
+//  warp 10    L_i and D_i of each query block into shared memory (two stages).
+//  warp 11    no role (it completes the TMA/MMA warpgroup).
 //
 // Per query block the MMA thread issues, at d = 128, dV_i, S_(i+1), dK_i,
 // dQ_i, dP_(i+1) (dQ_i shares dP^T's TMEM columns); at d = 64, where S^T, P^T,
 // dP^T and dQ each have columns of their own, dV_i and S_(i+1), then
 // dP_(i+1) as soon as the key rows have read dP_i, then dK_i and dQ_i, so that
 // the next S and dP are ready before the key rows need them.
-//  warp 9     TMEM allocation and the single MMA-issuing thread.
-//  warp 10    L_i and D_i of each query block into shared memory (two stages).
-//  warp 11    no role (it completes the TMA/MMA warpgroup).
 #include <cuda_bf16.h>
 
 #include <algorithm>
