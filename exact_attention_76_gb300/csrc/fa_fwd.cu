@@ -33,6 +33,10 @@
 // handed over in two 64-key halves: PV over the first half runs while the
 // warpgroup exponentiates the second.
 //
+// FP8 at d = 128 splits S_t into two 64-key halves with P over the second, so
+// that the next block's first half is computed while the softmax runs (see
+// FwdCfg::kSplitS).
+//
 // At d = 64 (O takes half the columns) P_t has TMEM columns of its own, and
 // the order changes: the warpgroup signals s_free as soon as S_t(j) is in its
 // registers, the MMA thread then issues S_t(j+1) at once, and PV_t(j) after
@@ -49,7 +53,7 @@
 // computed; the e4m3 factor 2^4 is folded into the exponent.
 //
 // TMEM columns: S_0 [0,128), S_1 [128,256) (at d = 128, P_t in the first 64
-// columns of S_t for bf16, the first 32 for e4m3), O_0 [256,256+D),
+// columns of S_t for bf16, columns 64-95 for e4m3), O_0 [256,256+D),
 // O_1 [256+D,256+2D), and at d = 64 P_0 [384,448), P_1 [448,512).
 // Q stays in shared memory: an M = 128, N = 128 product with both operands in
 // shared memory uses the full shared-memory operand bandwidth, not more
@@ -200,6 +204,16 @@ struct FwdCfg {
   // N = 8192 and 16384, +10 % in FP8, +3-8 % at N = 512 and 1024); at d = 128
   // P is written over S_t.
   static constexpr bool kEarlyS = (D == 64);
+  // FP8 at d = 128 computes S_t in two 64-key halves: P_t(j) (32 columns) is
+  // written over the second half's columns, so the first half of S_t(j+1) is
+  // issued as soon as the warpgroup has read S_t(j)'s first half, and only the
+  // second half follows PV_t(j) in issue order; the warpgroup reduces the
+  // first half's maximum while the second is computed.  N = 64 products run
+  // at two thirds of the N = 128 rate, so S costs 1.5x the tensor time:
+  // measured +5-6 % in FP8 (whose tensor pipe has room), -8 to -11 % in bf16.
+  static constexpr bool kSplitS = FP8 && D == 128;
+  static constexpr uint32_t kIdescSHalf =
+      FP8 ? idesc_e4m3(128, kBN / 2, false, false) : idesc_bf16(128, kBN / 2, false, false);
   static constexpr uint32_t kTmP = kEarlyS ? 384 : 0;  // + t * 64
   static_assert(!kEarlyS || kTmO + 2 * D <= kTmP, "TMEM columns");
   static_assert(D == 64 || D == 128, "head dim");
@@ -219,6 +233,7 @@ struct FwdSmem {
   uint64_t p_half[2];
   uint64_t o_done[2];
   uint64_t s_free[2];
+  uint64_t s_full_b[2];
   uint64_t drain;
   uint32_t tmem_base;
   float vmax_part[2][4];
@@ -278,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.p_half[t], kBM);
       mbar_init(&sh.o_done[t], 1);
       mbar_init(&sh.s_free[t], kBM);
+      mbar_init(&sh.s_full_b[t], 1);
     }
     mbar_init(&sh.drain, 1);
     fence_barrier_init();
@@ -348,10 +364,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(&sh.s_full[t]);
       };
+      // Half h of S_t (keys 64 h .. 64 h + 63 of the block) into S_t's columns
+      // 64 h .. 64 h + 63; completion on s_full (h = 0) or s_full_b (h = 1).
+      auto issue_s_half = [&](int t, int slot, int h) {
+        const uint64_t a0 = sdesc_advance(q_desc, t * C::kTileBytes);
+        const uint64_t b0 = sdesc_advance(k_desc, slot * C::kTileBytes + h * (kBN / 2) * C::kSwz);
+#pragma unroll
+        for (int kk = 0; kk < C::kQKSteps; ++kk) {
+          const uint32_t off = (kk / C::kStepsPerBlock) * C::kBlockBytes + (kk % C::kStepsPerBlock) * 32;
+          issue_mma(FP8, tmem + C::kTmS + t * kBN + h * (kBN / 2), sdesc_advance(a0, off), sdesc_advance(b0, off),
+                    C::kIdescSHalf, kk > 0);
+        }
+        tc_commit(h == 0 ? &sh.s_full[t] : &sh.s_full_b[t]);
+      };
       // O_t += P_t V_j over the K steps [k0, k1) of the block (P over S_t).
       auto issue_pv = [&](int t, int slot, bool acc, int k0, int k1) {
         const uint64_t b0 = sdesc_advance(v_desc, slot * C::kTileBytes);
-        const uint32_t a_tm = C::kEarlyS ? tmem + C::kTmP + t * 64 : tmem + C::kTmS + t * kBN;
+        const uint32_t a_tm = C::kEarlyS ? tmem + C::kTmP + t * 64
+                                         : tmem + C::kTmS + t * kBN + (C::kSplitS ? kBN / 2 : 0);
         const uint32_t d_tm = tmem + C::kTmO + t * D;
 #pragma unroll
         for (int kk = k0; kk < k1; ++kk)
@@ -374,7 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (len[t] > 0 && j_lo[t] == j_begin) issue_s(t, k_load(j_begin) % C::kSlots);
+          if (len[t] > 0 && j_lo[t] == j_begin) {
+            if constexpr (C::kSplitS) {
+              issue_s_half(t, k_load(j_begin) % C::kSlots, 0);
+              issue_s_half(t, k_load(j_begin) % C::kSlots, 1);
+            } else {
+              issue_s(t, k_load(j_begin) % C::kSlots);
+            }
+          }
         tc_commit(&sh.kv_empty[k_load(j_begin) % C::kSlots]);
       }
       for (int j = j_begin; ok && j < n_max; ++j) {
@@ -416,6 +453,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_pv(t, v_idx % C::kSlots, u > 0, C::kSplitP ? C::kPVSteps / 2 : 0, C::kPVSteps);
             tc_commit(&sh.o_done[t]);
+          }
+          if (!ok) break;
+          if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
+          if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
+          continue;
+        }
+        if constexpr (C::kSplitS) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok) break;
+            const int u = j - j_lo[t];
+            const bool next = u + 1 >= 0 && u + 1 < len[t];
+            // The first half of S_t(u+1) once the warpgroup has read S_t(u)'s first half ...
+            if (next && u >= 0) {
+              ok = mbar_wait<true>(&sh.s_free[t], u & 1, &sh.abort, &g_err_fwd);
+              if (ok && !k_ready) {
+                ok = wait_load(k_idx);
+                k_ready = true;
+              }
+              if (!ok) break;
+              tc_fence_after();
+              issue_s_half(t, k_idx % C::kSlots, 0);
+            }
+            // ... PV_t(u) once it wrote P_t(u) over S_t(u)'s second half ...
+            if (u >= 0 && u < len[t]) {
+              if (!v_ready) {
+                ok = wait_load(v_idx);
+                v_ready = true;
+              }
+              if constexpr (C::kSplitP) {
+                ok = ok && wait_p(&sh.p_half[t], u);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, v_idx % C::kSlots, u > 0, 0, C::kPVSteps / 2);
+              }
+              ok = ok && wait_p(&sh.p_full[t], u);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(t, v_idx % C::kSlots, u > 0, C::kSplitP ? C::kPVSteps / 2 : 0, C::kPVSteps);
+              tc_commit(&sh.o_done[t]);
+            }
+            // ... and right behind it the second half of S_t(u+1) into P_t(u)'s
+            // columns (both halves when the tile starts at block j + 1).
+            if (next) {
+              if (!k_ready) {
+                ok = wait_load(k_idx);
+                k_ready = true;
+                if (!ok) break;
+                tc_fence_after();
+              }
+              if (u + 1 == 0) issue_s_half(t, k_idx % C::kSlots, 0);
+              issue_s_half(t, k_idx % C::kSlots, 1);
+            }
           }
           if (!ok) break;
           if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
@@ -470,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_base + C::kTmS + t * kBN;
     const uint32_t o_col = tmem + lane_base + C::kTmO + t * D;
-    const uint32_t p_col = C::kEarlyS ? tmem + lane_base + C::kTmP + t * 64 : s_col;
+    const uint32_t p_col = C::kEarlyS ? tmem + lane_base + C::kTmP + t * 64 : s_col + (C::kSplitS ? kBN / 2 : 0);
     const int row_g = q0 + t * kBM + r;
     const int jlo_t = t ? j_lo[1] : j_lo[0];
     const int nt = t ? len[1] : len[0];
@@ -519,7 +609,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       float s0[64], s1[64];
-      {
+      const int key0 = j * kBN;
+      const bool need_mask = (causal && key0 + kBN - 1 > q0 + t * kBM) || (key0 + kBN > N) ||
+                             (WIN && key0 < q0 + t * kBM + kBM - window);
+      const int lim = causal ? min(row_g, N - 1) : N - 1;  // last visible key
+      const int lo = WIN ? row_g - window + 1 : 0;          // first visible key
+      auto mask_half = [&](float (&sh_)[64], int k0) {
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (k0 + i > lim || (WIN && k0 + i < lo)) sh_[i] = -INFINITY;
+        }
+      };
+      // Row maximum: independent chains of three-input maxima (measured against
+      // two-input ones: +3 % at d = 128 without a mask, the same elsewhere),
+      // then the block's candidate in log2 units (c0, c1 > 0 preserve the
+      // order within each half).
+      float mx[4];
+      auto max_half = [&](const float (&sh_)[64], float& a, float& b) {
+        a = sh_[0];
+        b = sh_[1];
+#pragma unroll
+        for (int i = 2; i < 62; i += 4) {
+          a = fmax3f(a, sh_[i], sh_[i + 2]);
+          b = fmax3f(b, sh_[i + 1], sh_[i + 3]);
+        }
+        a = fmaxf(a, sh_[62]);
+        b = fmaxf(b, sh_[63]);
+      };
+      if constexpr (C::kSplitS) {
+        // First half: read, free its columns for S_t(u+1)'s first half, reduce;
+        // then the second half, which follows PV_t(u-1) in issue order.
+        {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(s_col, ra);
+          tmem_ld32(s_col + 32, rb);
+          tmem_ld_wait(ra);
+          tmem_ld_wait(rb);
+          tc_fence_before();
+          mbar_arrive(&sh.s_free[t]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            s0[i] = __uint_as_float(ra[i]);
+            s0[32 + i] = __uint_as_float(rb[i]);
+          }
+        }
+        mask_half(s0, key0);
+        max_half(s0, mx[0], mx[1]);
+        ok = mbar_wait<true>(&sh.s_full_b[t], u & 1, &sh.abort, &g_err_fwd);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          uint32_t rc[32], rd[32];
+          tmem_ld32(s_col + 64, rc);
+          tmem_ld32(s_col + 96, rd);
+          tmem_ld_wait(rc);
+          tmem_ld_wait(rd);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            s1[i] = __uint_as_float(rc[i]);
+            s1[32 + i] = __uint_as_float(rd[i]);
+          }
+        }
+        mask_half(s1, key0 + 64);
+        max_half(s1, mx[2], mx[3]);
+      } else {
         uint32_t ra[32], rb[32], rc[32], rd[32];
         tmem_ld32(s_col, ra);
         tmem_ld32(s_col + 32, rb);
@@ -540,35 +694,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           s1[i] = __uint_as_float(rc[i]);
           s1[32 + i] = __uint_as_float(rd[i]);
         }
-      }
-      const int key0 = j * kBN;
-      const bool need_mask = (causal && key0 + kBN - 1 > q0 + t * kBM) || (key0 + kBN > N) ||
-                             (WIN && key0 < q0 + t * kBM + kBM - window);
-      if (need_mask) {
-        const int lim = causal ? min(row_g, N - 1) : N - 1;  // last visible key
-        const int lo = WIN ? row_g - window + 1 : 0;          // first visible key
+        mask_half(s0, key0);
+        mask_half(s1, key0 + 64);
+        mx[0] = s0[0];
+        mx[1] = s0[1];
+        mx[2] = s1[0];
+        mx[3] = s1[1];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          if (key0 + i > lim || (WIN && key0 + i < lo)) s0[i] = -INFINITY;
-          if (key0 + 64 + i > lim || (WIN && key0 + 64 + i < lo)) s1[i] = -INFINITY;
+        for (int i = 2; i < 62; i += 4) {
+          mx[0] = fmax3f(mx[0], s0[i], s0[i + 2]);
+          mx[1] = fmax3f(mx[1], s0[i + 1], s0[i + 3]);
+          mx[2] = fmax3f(mx[2], s1[i], s1[i + 2]);
+          mx[3] = fmax3f(mx[3], s1[i + 1], s1[i + 3]);
         }
+        mx[0] = fmaxf(mx[0], s0[62]);
+        mx[1] = fmaxf(mx[1], s0[63]);
+        mx[2] = fmaxf(mx[2], s1[62]);
+        mx[3] = fmaxf(mx[3], s1[63]);
       }
-      // Row maximum: four independent chains of three-input maxima (measured
-      // against two-input ones: +3 % at d = 128 without a mask, the same
-      // elsewhere), then the block's candidate in log2 units (c0, c1 > 0
-      // preserve the order within each half).
-      float mx[4] = {s0[0], s0[1], s1[0], s1[1]};
-#pragma unroll
-      for (int i = 2; i < 62; i += 4) {
-        mx[0] = fmax3f(mx[0], s0[i], s0[i + 2]);
-        mx[1] = fmax3f(mx[1], s0[i + 1], s0[i + 3]);
-        mx[2] = fmax3f(mx[2], s1[i], s1[i + 2]);
-        mx[3] = fmax3f(mx[3], s1[i + 1], s1[i + 3]);
-      }
-      mx[0] = fmaxf(mx[0], s0[62]);
-      mx[1] = fmaxf(mx[1], s0[63]);
-      mx[2] = fmaxf(mx[2], s1[62]);
-      mx[3] = fmaxf(mx[3], s1[63]);
       const float m_cand = fmaxf(fmaxf(mx[0], mx[1]) * c0, fmaxf(mx[2], mx[3]) * c1);
       float alpha = 1.0f;
       bool raise = false;
