@@ -208,9 +208,9 @@ struct FwdCfg {
   // written over the second half's columns, so the first half of S_t(j+1) is
   // issued as soon as the warpgroup has read S_t(j)'s first half, and only the
   // second half follows PV_t(j) in issue order; the warpgroup reduces the
-  // first half's maximum while the second is computed.  N = 64 products run
-  // at two thirds of the N = 128 rate, so S costs 1.5x the tensor time:
-  // measured +5-6 % in FP8 (whose tensor pipe has room), -8 to -11 % in bf16.
+  // first half's maximum while the second is computed.  Measured +5-6 % in
+  // FP8 (tensor-pipe active cycles per launch unchanged); bf16, whose PV is
+  // twice as long, measured 8-11 % slower with the same split.
   static constexpr bool kSplitS = FP8 && D == 128;
   static constexpr uint32_t kIdescSHalf =
       FP8 ? idesc_e4m3(128, kBN / 2, false, false) : idesc_bf16(128, kBN / 2, false, false);
