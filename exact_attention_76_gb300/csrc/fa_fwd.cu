@@ -454,12 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_pv(t, v_idx % C::kSlots, u > 0, C::kSplitP ? C::kPVSteps / 2 : 0, C::kPVSteps);
             tc_commit(&sh.o_done[t]);
           }
-          if (!ok) break;
-          if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
-          if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
-          continue;
-        }
-        if constexpr (C::kSplitS) {
+        } else if constexpr (C::kSplitS) {
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (!ok) break;
@@ -507,42 +502,39 @@ __global__ void __launch_bounds__(kThreads, 1)
               issue_s_half(t, k_idx % C::kSlots, 1);
             }
           }
-          if (!ok) break;
-          if (k_ready) tc_commit(&sh.kv_empty[k_idx % C::kSlots]);
-          if (v_ready) tc_commit(&sh.kv_empty[v_idx % C::kSlots]);
-          continue;
-        }
+        } else {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (!ok) break;
-          const int u = j - j_lo[t];
-          // PV_t(u) once the warpgroup wrote P_t(u) over S_t(u) ...
-          if (u >= 0 && u < len[t]) {
-            if (!v_ready) {
-              ok = wait_load(v_idx);
-              v_ready = true;
-            }
-            if constexpr (C::kSplitP) {  // keys 0-63 as soon as their P is there
-              ok = ok && wait_p(&sh.p_half[t], u);
-              if (!ok) break;
-              tc_fence_after();
-              issue_pv(t, v_idx % C::kSlots, u > 0, 0, C::kPVSteps / 2);
-            }
-            ok = ok && wait_p(&sh.p_full[t], u);
+          for (int t = 0; t < 2; ++t) {
             if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, v_idx % C::kSlots, u > 0, C::kSplitP ? C::kPVSteps / 2 : 0, C::kPVSteps);
-            tc_commit(&sh.o_done[t]);
-          }
-          // ... and right behind it S_t(u+1) into the same columns.
-          if (u + 1 >= 0 && u + 1 < len[t]) {
-            if (!k_ready) {
-              ok = wait_load(k_idx);
-              k_ready = true;
+            const int u = j - j_lo[t];
+            // PV_t(u) once the warpgroup wrote P_t(u) over S_t(u) ...
+            if (u >= 0 && u < len[t]) {
+              if (!v_ready) {
+                ok = wait_load(v_idx);
+                v_ready = true;
+              }
+              if constexpr (C::kSplitP) {  // keys 0-63 as soon as their P is there
+                ok = ok && wait_p(&sh.p_half[t], u);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, v_idx % C::kSlots, u > 0, 0, C::kPVSteps / 2);
+              }
+              ok = ok && wait_p(&sh.p_full[t], u);
               if (!ok) break;
               tc_fence_after();
+              issue_pv(t, v_idx % C::kSlots, u > 0, C::kSplitP ? C::kPVSteps / 2 : 0, C::kPVSteps);
+              tc_commit(&sh.o_done[t]);
             }
-            issue_s(t, k_idx % C::kSlots);
+            // ... and right behind it S_t(u+1) into the same columns.
+            if (u + 1 >= 0 && u + 1 < len[t]) {
+              if (!k_ready) {
+                ok = wait_load(k_idx);
+                k_ready = true;
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(t, k_idx % C::kSlots);
+            }
           }
         }
         if (!ok) break;
