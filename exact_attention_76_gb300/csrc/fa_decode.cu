@@ -119,6 +119,10 @@ __global__ void __launch_bounds__(kDecThreads, 3)
     }
     fence_barrier_init();
   }
+  // Set-up done: the next kernel may start launching; q, the cache and the
+  // workspace are touched only after the kernels before this one completed.
+  pdl_launch_dependents();
+  pdl_wait_prior();
   // q of the group, fp32, times scale * log2 e, each quarter row padded so that
   // the four quarters fall in different banks.
   for (int i = threadIdx.x; i < g * D; i += kDecThreads) {
@@ -340,6 +344,8 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float* __res
                                                               __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                                               int rows, int nsplit) {
   constexpr int E = D / 32;
+  pdl_launch_dependents();
+  pdl_wait_prior();  // the chunks' partials come from the kernel before
   const int row = static_cast<int>(blockIdx.x) * 8 + static_cast<int>(warp_id());
   if (row >= rows) return;
   const size_t stride = D + 4;
@@ -362,6 +368,20 @@ __global__ void __launch_bounds__(256) fa_decode_merge_kernel(const float* __res
   if (lane_id() == 0) lse[row] = m * 0.69314718055994531f + logf(l);
 }
 
+// Both decode kernels and the merge are launched with programmatic stream
+// serialization: each signals its dependents after its set-up and waits for
+// the kernels before it only where it first touches memory, so the merge's
+// launch overlaps the decode kernel's last CTAs and the next call's set-up
+// overlaps the merge.
+template <int D>
+fa_status launch_merge(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
+  const int rows = a.B * a.H;
+  return launch_pdl(fa_decode_merge_kernel<D>, dim3((rows + 7) / 8), dim3(256), 0, s, a.part,
+                    static_cast<__nv_bfloat16*>(a.o), a.lse, rows, pl.nsplit) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_LAUNCH;
+}
+
 template <int D, int G>
 fa_status launch_decode_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
   using Cf = DecCfg<D>;
@@ -377,12 +397,10 @@ fa_status launch_decode_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStre
       cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return FA_ERR_LAUNCH;
   const dim3 grid(static_cast<unsigned>(pl.nsplit), static_cast<unsigned>(BHkv));
-  kern<<<grid, kDecThreads, smem, s>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.q), a.part, a.H, a.Hkv, a.N,
-                                       pl.chunk, pl.nsplit, a.scale * 1.4426950408889634f);
-  const int rows = a.B * a.H;
-  fa_decode_merge_kernel<D><<<(rows + 7) / 8, 256, 0, s>>>(a.part, static_cast<__nv_bfloat16*>(a.o), a.lse, rows,
-                                                          pl.nsplit);
-  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  if (launch_pdl(kern, grid, dim3(kDecThreads), smem, s, mk, mv, static_cast<const __nv_bfloat16*>(a.q), a.part, a.H,
+                 a.Hkv, a.N, pl.chunk, pl.nsplit, a.scale * 1.4426950408889634f) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return launch_merge<D>(a, pl, s);
 }
 
 
@@ -473,6 +491,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(&sh.drain, 1);
     fence_barrier_init();
   }
+  if (warp == 5) tmem_alloc(&sh.tmem_base, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  // Set-up done: the next kernel may start launching; q, the cache and the
+  // workspace are touched only after the kernels before this one completed.
+  pdl_launch_dependents();
+  pdl_wait_prior();
   // Q of the group as a 16-row K-major bf16 tile (rows past g are zero).
   for (int i = t; i < kTcN * D; i += kTcThreads) {
     const int h = i / D, e = i % D;
@@ -480,11 +507,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     *reinterpret_cast<__nv_bfloat16*>(s_qp + kmaj_off(h, e, kTcN)) = val;
   }
   fence_proxy_async_smem();  // generic-proxy stores -> tensor core reads
-  if (warp == 5) tmem_alloc(&sh.tmem_base, 256);
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sh.tmem_base;
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
@@ -679,12 +702,10 @@ fa_status launch_decode_tc_impl(const DecodeArgs& a, const DecodePlan& pl, cudaS
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem) != cudaSuccess)
     return FA_ERR_LAUNCH;
   const dim3 grid(static_cast<unsigned>(pl.nsplit), static_cast<unsigned>(BHkv));
-  kern<<<grid, kTcThreads, kTcSmem, s>>>(mk, mv, static_cast<const __nv_bfloat16*>(a.q), a.part, a.H, a.Hkv, a.N,
-                                         pl.chunk, pl.nsplit, a.scale * 1.4426950408889634f);
-  const int rows = a.B * a.H;
-  fa_decode_merge_kernel<D><<<(rows + 7) / 8, 256, 0, s>>>(a.part, static_cast<__nv_bfloat16*>(a.o), a.lse, rows,
-                                                          pl.nsplit);
-  return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  if (launch_pdl(kern, grid, dim3(kTcThreads), kTcSmem, s, mk, mv, static_cast<const __nv_bfloat16*>(a.q), a.part,
+                 a.H, a.Hkv, a.N, pl.chunk, pl.nsplit, a.scale * 1.4426950408889634f) != cudaSuccess)
+    return FA_ERR_LAUNCH;
+  return launch_merge<D>(a, pl, s);
 }
 
 fa_status launch_decode_tc(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t s) {
