@@ -408,40 +408,48 @@ fa_status launch_decode_impl(const DecodeArgs& a, const DecodePlan& pl, cudaStre
 // Grouped heads (2..16 query heads per key/value head): the score and
 // P.V products are real contractions over the group, (keys x d)(d x heads)
 // and (d x keys)(keys x heads), so they go to the tensor cores, which leaves
-// the kernel bound by the cache read again.
-//   warps 0-3 : one key of a 128-key tile per thread (TMEM lane); pass 1
-//               reads S^T and keeps per-head maxima, pass 2 forms P and
-//               writes it to shared memory as the B operand of P.V; at the
-//               end thread t reads column d = t of O^T.
-//   warp 4    : TMA producer (K tiles, then V tiles, 3-slot ring).
+// the kernel bound by the cache read again.  A chunk's tiles are processed
+// one at a time with the online softmax of "FLASH-ATTN", FlashAttention-2
+// (per head a running maximum, raised only past a threshold, and a running
+// sum), so K and V tiles stream interleaved and a chunk may be any length.
+//   warps 0-3 : one key of a 128-key tile per thread (TMEM lane): per tile
+//               the per-head maximum over the tile's keys, then P into shared
+//               memory as the B operand of P.V; thread t also owns row d = t
+//               of O^T, which it rescales when a head's maximum is raised,
+//               and reads out at the end.
+//   warp 4    : TMA producer: K_0, K_1, V_0, K_2, V_1, ... through a 3-slot
+//               ring (the next tile's scores are computed during this one's
+//               softmax).
 //   warp 5    : TMEM allocation and the MMA-issuing thread.
 // S^T = K Q^T (M = 128 keys, N = 16 padded heads, A = K tile K-major, B = Q
-// K-major) in TMEM columns 16 t; O^T += V^T P^T (M = 128 rows of d, N = 16,
-// A = V tile read MN-major, B = P K-major) in columns 128.. .  At d = 64 a
-// ring slot keeps its 128-row size: the product's rows 64..127 read the
-// slot's unused second half and are never read back.
+// K-major) in TMEM columns 16 (t & 1); O^T += V^T P^T (M = 128 rows of d,
+// N = 16, A = V tile read MN-major, B = P K-major) in columns 128.. .  At
+// d = 64 a ring slot keeps its 128-row size: the product's rows 64..127 read
+// the slot's unused second half and are never read back.
 constexpr int kTcThreads = 192;
 constexpr int kTcTile = 128;           // keys per tile
 constexpr int kTcSlots = 3;
 constexpr int kTcTileBytes = kTcTile * 128 * 2;  // 32 KB: a 128-key tile at d = 128 (slot size)
 constexpr int kTcBlockBytes = kTcTile * 128;     // one 64-column block of a tile
-constexpr int kTcMaxTiles = 8;         // chunk <= 1024 keys
 constexpr int kTcN = 16;               // padded heads
 constexpr int kTcPBytes = kTcN * kTcTile * 2;    // 4 KB: P of one tile (16 x 128 bf16)
 constexpr int kTcQBytes = kTcN * 128 * 2;        // 4 KB
 constexpr uint32_t kTcTmO = 128;
+constexpr float kTcTauLog2 = 8.0f;     // P <= 2^8 between raises of a head's maximum
 constexpr int kTcSmem = 1024 + kTcSlots * kTcTileBytes + 2 * kTcPBytes + kTcQBytes;
 
 struct DecTcSmem {
   uint64_t full[kTcSlots];
   uint64_t empty[kTcSlots];
-  uint64_t s_full[kTcMaxTiles];
+  uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t p_empty[2];
+  uint64_t pv_done;
   uint64_t o_done;
   uint64_t drain;
   uint32_t tmem_base;
-  float red[4][kTcN];
+  float red[2][4][kTcN];   // per-tile maxima of the four warps (double-buffered by tile)
+  float lred[4][kTcN];     // the warps' row sums at the end
   float m[kTcN];
   float l[kTcN];
   CtaAbort abort;
@@ -452,6 +460,11 @@ struct DecTcSmem {
 __device__ __forceinline__ int kmaj_off(int r, int e, int rows) {
   return (e >> 6) * rows * 128 + r * 128 + ((((e & 63) >> 3) ^ (r & 7)) << 4) + ((e & 7) << 1);
 }
+
+// Ring order of a chunk's n tiles: K_0, then for each tile t, K_(t+1) (if
+// any) and V_t.  Position of K_t and V_t in that order:
+__device__ __forceinline__ int tc_k_pos(int t) { return t == 0 ? 0 : 2 * t - 1; }
+__device__ __forceinline__ int tc_v_pos(int t, int n) { return t < n - 1 ? 2 * t + 2 : 2 * t + 1; }
 
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -482,11 +495,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sh.full[i], 1);
       mbar_init(&sh.empty[i], 1);
     }
-    for (int i = 0; i < kTcMaxTiles; ++i) mbar_init(&sh.s_full[i], 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_full[i], 128);
       mbar_init(&sh.p_empty[i], 1);
     }
+    mbar_init(&sh.pv_done, 1);
     mbar_init(&sh.o_done, 1);
     mbar_init(&sh.drain, 1);
     fence_barrier_init();
@@ -515,12 +529,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
       int issued = 0;
-      for (int it = 0; it < 2 * n_tiles && !sh.abort.flag; ++it) {
+      for (int i = 0; i < 2 * n_tiles && !sh.abort.flag; ++i) {
         const int slot = issued % kTcSlots;
         const int round = issued / kTcSlots;
         if (round > 0 && !mbar_wait<true>(&sh.empty[slot], (round - 1) & 1, &sh.abort, &g_err_dec)) break;
-        const bool is_k = it < n_tiles;
-        const int key0 = key_begin + (is_k ? it : it - n_tiles) * kTcTile;
+        // position i -> (K or V, tile), the inverse of tc_k_pos / tc_v_pos
+        const bool is_k = i == 0 || (i != 2 * n_tiles - 1 && (i & 1));
+        const int tile = i == 0 ? 0 : (i == 2 * n_tiles - 1 ? n_tiles - 1 : (is_k ? (i + 1) / 2 : (i - 2) / 2));
+        const int key0 = key_begin + tile * kTcTile;
         mbar_arrive_expect_tx(&sh.full[slot], kTcTile * D * 2);
         for (int cb = 0; cb < D / 64; ++cb)
           tma_load_3d(s_ring + slot * kTcTileBytes + cb * kTcBlockBytes, is_k ? &map_k : &map_v, cb * 64, key0, bkv,
@@ -545,26 +561,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t q_k = sdesc_sw128(smem_u32(s_qp), 16, 1024);
       const uint64_t p_k = sdesc_sw128(smem_u32(s_p), 16, 1024);
       bool ok = true;
-      int used = 0;
-      for (int tile = 0; ok && tile < n_tiles; ++tile, ++used) {
-        const int slot = used % kTcSlots;
-        ok = mbar_wait<true>(&sh.full[slot], (used / kTcSlots) & 1, &sh.abort, &g_err_dec);
-        if (!ok) break;
+      // S^T of tile u into columns 16 (u & 1); the ring is consumed in order.
+      auto issue_s = [&](int u) {
+        const int pos = tc_k_pos(u);
+        const int slot = pos % kTcSlots;
+        ok = mbar_wait<true>(&sh.full[slot], (pos / kTcSlots) & 1, &sh.abort, &g_err_dec);
+        if (!ok) return;
         tc_fence_after();
         const uint64_t a0 = sdesc_advance(ring_k, slot * kTcTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          mma_bf16_ss(tmem + tile * kTcN, sdesc_advance(a0, (kk >> 2) * kTcBlockBytes + (kk & 3) * 32),
+          mma_bf16_ss(tmem + (u & 1) * kTcN, sdesc_advance(a0, (kk >> 2) * kTcBlockBytes + (kk & 3) * 32),
                       sdesc_advance(q_k, (kk >> 2) * (kTcN * 128) + (kk & 3) * 32), kIdS, kk > 0);
         }
-        tc_commit(&sh.s_full[tile]);
+        tc_commit(&sh.s_full[u & 1]);
         tc_commit(&sh.empty[slot]);
-      }
-      for (int tile = 0; ok && tile < n_tiles; ++tile, ++used) {
-        const int slot = used % kTcSlots;
-        const int b = tile & 1;
-        ok = mbar_wait<true>(&sh.full[slot], (used / kTcSlots) & 1, &sh.abort, &g_err_dec) &&
-             mbar_wait<true>(&sh.p_full[b], (tile >> 1) & 1, &sh.abort, &g_err_dec);
+      };
+      issue_s(0);
+      if (ok && n_tiles > 1) issue_s(1);
+      for (int u = 0; ok && u < n_tiles; ++u) {
+        const int b = u & 1;
+        const int pos = tc_v_pos(u, n_tiles);
+        const int slot = pos % kTcSlots;
+        // P_u written (and S^T_u read) by the key warps, V_u landed
+        ok = mbar_wait<true>(&sh.p_full[b], (u >> 1) & 1, &sh.abort, &g_err_dec) &&
+             mbar_wait<true>(&sh.full[slot], (pos / kTcSlots) & 1, &sh.abort, &g_err_dec);
         if (!ok) break;
         tc_fence_after();
         const uint64_t a0 = sdesc_advance(ring_mn, slot * kTcTileBytes);
@@ -572,10 +593,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           mma_bf16_ss(tmem + kTcTmO, sdesc_advance(a0, kk * 2048),
-                      sdesc_advance(b0, (kk >> 2) * (kTcN * 128) + (kk & 3) * 32), kIdPV, (tile > 0 || kk > 0) ? 1u : 0u);
+                      sdesc_advance(b0, (kk >> 2) * (kTcN * 128) + (kk & 3) * 32), kIdPV, (u > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&sh.p_empty[b]);
         tc_commit(&sh.empty[slot]);
+        tc_commit(&sh.pv_done);
+        if (u + 2 < n_tiles) issue_s(u + 2);  // into the columns S^T_u has left
       }
       if (ok) tc_commit(&sh.o_done);
       tc_commit(&sh.drain);
@@ -584,65 +607,91 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ keys (lanes)
+    // Every thread takes every named barrier below; a failed wait only clears
+    // `ok`, and the barriers that combine `ok` make all four warps stop
+    // together.
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok = true;
-    float m[kTcN];
+    float m[kTcN], l[kTcN];  // per head: reference maximum (log2 units), this thread's partial sum
 #pragma unroll
-    for (int h = 0; h < kTcN; ++h) m[h] = -INFINITY;
-    // pass 1: per-head maxima of x = s * scale * log2 e
-    for (int tile = 0; tile < n_tiles; ++tile) {
-      ok = ok && mbar_wait<true>(&sh.s_full[tile], 0, &sh.abort, &g_err_dec);
-      ok = __all_sync(0xffffffffu, ok);
+    for (int h = 0; h < kTcN; ++h) {
+      m[h] = 0.f;
+      l[h] = 0.f;
+    }
+    for (int u = 0; u < n_tiles; ++u) {
+      const int b = u & 1;
+      const bool valid = key_begin + u * kTcTile + t < key_end;
+      float x[kTcN];
+      ok = ok && mbar_wait<true>(&sh.s_full[b], (u >> 1) & 1, &sh.abort, &g_err_dec);
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + b * kTcN, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int h = 0; h < kTcN; ++h) x[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
+      } else {
+#pragma unroll
+        for (int h = 0; h < kTcN; ++h) x[h] = -INFINITY;
+      }
+      // the tile's maximum per head over its 128 keys: warp, then the four warps
+      float mt[kTcN];
+#pragma unroll
+      for (int h = 0; h < kTcN; ++h) {
+        mt[h] = x[h];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], off));
+      }
+      if (lane_id() == 0) {
+#pragma unroll
+        for (int h = 0; h < kTcN; ++h) sh.red[b][warp][h] = mt[h];
+      }
+      // (sh.red[b] is written again two tiles on, after every thread has
+      // passed the next tile's barrier, so after this tile's reads)
+      ok = named_bar_and(1, 128, ok);
       if (!ok) break;
-      tc_fence_after();
-      uint32_t r[16];
-      tmem_ld16(tmem + lane_base + tile * kTcN, r);
-      tmem_ld_wait(r);
-      if (key_begin + tile * kTcTile + t < key_end) {
+      bool raise = false;
+      float alpha[kTcN];
 #pragma unroll
-        for (int h = 0; h < kTcN; ++h) m[h] = fmaxf(m[h], __uint_as_float(r[h]) * scale_log2);
+      for (int h = 0; h < kTcN; ++h) {
+        const float mm = fmaxf(fmaxf(sh.red[b][0][h], sh.red[b][1][h]), fmaxf(sh.red[b][2][h], sh.red[b][3][h]));
+        alpha[h] = 1.0f;
+        if (u == 0) {
+          m[h] = mm == -INFINITY ? 0.0f : mm;  // padded heads (and no visible key) use 0
+        } else if (mm > m[h] + kTcTauLog2) {
+          alpha[h] = ex2_approx(m[h] - mm);
+          m[h] = mm;
+          raise = true;
+        }
       }
-    }
-    // maxima over the 128 keys of the threads: warp, then the four warps
+      // (the same values in every thread: `raise` is uniform)
+      if (raise) {
+        // O^T is complete up to PV_(u-1); thread t rescales its row d = t
+        ok = mbar_wait<true>(&sh.pv_done, (u - 1) & 1, &sh.abort, &g_err_dec);
+        if (ok) {
+          tc_fence_after();
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_base + kTcTmO, r);
+          tmem_ld_wait(r);
 #pragma unroll
-    for (int h = 0; h < kTcN; ++h) {
+          for (int h = 0; h < kTcN; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * alpha[h]);
+          tmem_st16(tmem + lane_base + kTcTmO, r);
+          tmem_st_wait();
+        }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], off));
-    }
-    if (lane_id() == 0) {
-#pragma unroll
-      for (int h = 0; h < kTcN; ++h) sh.red[warp][h] = m[h];
-    }
-    named_bar_sync(1, 128);
-#pragma unroll
-    for (int h = 0; h < kTcN; ++h) {
-      const float mm = fmaxf(fmaxf(sh.red[0][h], sh.red[1][h]), fmaxf(sh.red[2][h], sh.red[3][h]));
-      m[h] = mm == -INFINITY ? 0.0f : mm;  // padded heads (and no visible key) use 0
-    }
-    named_bar_sync(1, 128);  // every thread has read sh.red before it is reused for l
-    // pass 2: P = 2^(x - m) into the B operand of P.V, and l = sum P
-    float l[kTcN];
-#pragma unroll
-    for (int h = 0; h < kTcN; ++h) l[h] = 0.f;
-    for (int tile = 0; ok && tile < n_tiles; ++tile) {
-      const int b = tile & 1;
-      uint32_t r[16];
-      tmem_ld16(tmem + lane_base + tile * kTcN, r);
-      tmem_ld_wait(r);
-      const bool valid = key_begin + tile * kTcTile + t < key_end;
-      if (tile >= 2) {  // the P.V two tiles back has read this buffer
-        ok = mbar_wait<true>(&sh.p_empty[b], ((tile >> 1) - 1) & 1, &sh.abort, &g_err_dec);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+        for (int h = 0; h < kTcN; ++h) l[h] *= alpha[h];
       }
+      if (ok && u >= 2)  // the P.V two tiles back has read this buffer
+        ok = mbar_wait<true>(&sh.p_empty[b], ((u >> 1) - 1) & 1, &sh.abort, &g_err_dec);
       uint8_t* pb = s_p + b * kTcPBytes;
 #pragma unroll
       for (int h = 0; h < kTcN; ++h) {
-        const float pv = valid ? ex2_approx(__uint_as_float(r[h]) * scale_log2 - m[h]) : 0.f;
+        const float pv = valid ? ex2_approx(x[h] - m[h]) : 0.f;
         l[h] += pv;
-        *reinterpret_cast<__nv_bfloat16*>(pb + kmaj_off(h, t, kTcN)) = __float2bfloat16_rn(pv);
+        if (ok) *reinterpret_cast<__nv_bfloat16*>(pb + kmaj_off(h, t, kTcN)) = __float2bfloat16_rn(pv);
       }
       fence_proxy_async_smem();
+      tc_fence_before();
       mbar_arrive(&sh.p_full[b]);
     }
 #pragma unroll
@@ -652,14 +701,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (lane_id() == 0) {
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h) sh.red[warp][h] = l[h];
+      for (int h = 0; h < kTcN; ++h) sh.lred[warp][h] = l[h];
     }
     const bool all_ok = named_bar_and(1, 128, ok);
     if (t == 0) {
 #pragma unroll
       for (int h = 0; h < kTcN; ++h) {
         sh.m[h] = m[h];
-        sh.l[h] = (sh.red[0][h] + sh.red[1][h]) + (sh.red[2][h] + sh.red[3][h]);
+        sh.l[h] = (sh.lred[0][h] + sh.lred[1][h]) + (sh.lred[2][h] + sh.lred[3][h]);
       }
     }
     named_bar_sync(1, 128);
@@ -720,15 +769,43 @@ DecodePlan decode_plan(int B, int H, int Hkv, int N, int d) {
   const int g = H / Hkv;
   const int gp = (g + 3) & ~3;
   const bool tc = use_tc(g, d);
-  const int tile = tc ? kTcTile : kDecTile;
-  // chunk keys: the score buffer holds chunk x gp floats (CUDA-core path) or
-  // the chunk's S^T tiles fit their TMEM columns (tensor-core path); at most
-  // 1024 keys
-  int cmax = tc ? kTcMaxTiles * kTcTile : (kDecScoreBytes / 4 / gp) / kDecTile * kDecTile;
+  const long long units = static_cast<long long>(B) * Hkv;
+  if (tc) {
+    // Any chunk length (one tile at a time): one resident wave of at most two
+    // CTAs per SM on 152 SMs, each streaming one chunk; past one wave, the
+    // split of each (batch, key/value head) with the fewest waves per unit of
+    // work.
+    constexpr long long kWave = 2 * 152;
+    const long long tiles = (N + kTcTile - 1) / kTcTile;
+    long long ns = 1;
+    if (units < kWave) {
+      ns = kWave / units;
+    } else {
+      double best = 1e30;
+      for (long long c = 1; c <= 4; ++c) {
+        const double cost = static_cast<double>((units * c + kWave - 1) / kWave) / static_cast<double>(c);
+        if (cost < best - 1e-9) {
+          best = cost;
+          ns = c;
+        }
+      }
+    }
+    if (ns > tiles) ns = tiles;
+    if (ns < 1) ns = 1;
+    long long ch = (N + ns - 1) / ns;
+    ch = (ch + kTcTile - 1) / kTcTile * kTcTile;
+    DecodePlan p;
+    p.chunk = static_cast<int>(ch);
+    p.nsplit = static_cast<int>((N + ch - 1) / ch);
+    return p;
+  }
+  // CUDA-core path: the chunk's scores (chunk x gp floats) fit the score
+  // buffer; at most 1024 keys.
+  const int tile = kDecTile;
+  int cmax = (kDecScoreBytes / 4 / gp) / kDecTile * kDecTile;
   if (cmax > 1024) cmax = 1024;
   // Enough CTAs to fill 4 per SM on 152 SMs where the keys allow chunks of at
   // least 256.
-  const long long units = static_cast<long long>(B) * Hkv;
   long long want = (4 * 152 + units - 1) / units;
   const long long by_min = (N + 255) / 256;
   if (want > by_min) want = by_min;

@@ -576,6 +576,32 @@ def test_decode_matches_oracle(d, N, H, Hkv):
     assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,Hkv", [(16, 8), (32, 8)])
+def test_decode_running_max_raised_within_a_chunk(d, H, Hkv):
+    # Keys whose scale grows along the cache (1 + 0.01 n) raise each head's
+    # running maximum by more than the rescale threshold about every second
+    # 128-key tile, and query scales that differ per head make the heads raise
+    # at different tiles; B * Hkv = 32 key/value heads split the cache into
+    # chunks of several tiles, so the rescale of the output accumulator inside
+    # a chunk is exercised.  The softmax is peaked, so O is held to the bound
+    # that follows from the arithmetic (bf16 P, relative 2^-9 per entry, and l
+    # from the unrounded values: 2^-8 max|V| in all; half an ulp of |O| from
+    # the bf16 output), as in the forward's rescale test.
+    B, N = 4, 4096
+    q, k, v = _decode_case(B, H, Hkv, N, d, seed=21 + H)
+    k = (k.float() * (1.0 + 0.01 * torch.arange(N, dtype=torch.float32))[None, None, :, None]).to(torch.bfloat16)
+    q = (q.float() * (0.5 + torch.arange(H, dtype=torch.float32) / H)[None, :, None]).to(torch.bfloat16)
+    scale = 1 / math.sqrt(d)
+    o, lse = api.fa_decode(q.cuda(), k.cuda(), v.cuda(), scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.decode(q, k, v, scale)
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(o_ref), 1e-30))) - 8)
+    bound = half_ulp + 2.0 ** -8 * float(v.float().abs().max()) + 1e-4
+    assert np.all(np.abs(f64(o) - o_ref) <= bound)
+    assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
+
+
 def test_decode_long_cache_and_reused_workspace():
     # 32768 keys per head in many chunks; the oracle's row costs O(N d), so every
     # head is checked.  The same workspace serves two different calls.
