@@ -455,6 +455,18 @@ struct DecTcSmem {
   CtaAbort abort;
 };
 
+// Named barrier that also returns the OR of `v` over the participating threads.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pin, pout;\n setp.ne.u32 pin, %1, 0;\n"
+      " barrier.cta.red.or.pred pout, %2, %3, pin;\n selp.u32 %0, 1, 0, pout;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // Byte offset of (row r, element e) in a K-major tile of `rows` rows stored as
 // 64-element (128-byte) column blocks with the 128-byte swizzle.
 __device__ __forceinline__ int kmaj_off(int r, int e, int rows) {
@@ -634,34 +646,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int h = 0; h < kTcN; ++h) x[h] = -INFINITY;
       }
-      // the tile's maximum per head over its 128 keys: warp, then the four warps
-      float mt[kTcN];
+      // Only a tile in which some key exceeds a head's reference by more than
+      // the threshold (and the first tile) needs the tile's maxima: one
+      // barrier tells every thread whether any did (a failed wait counts, so
+      // that the barrier below combines the status).
+      bool mine = u == 0 || !ok;
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h) {
-        mt[h] = x[h];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], off));
-      }
-      if (lane_id() == 0) {
-#pragma unroll
-        for (int h = 0; h < kTcN; ++h) sh.red[b][warp][h] = mt[h];
-      }
-      // (sh.red[b] is written again two tiles on, after every thread has
-      // passed the next tile's barrier, so after this tile's reads)
-      ok = named_bar_and(1, 128, ok);
-      if (!ok) break;
+      for (int h = 0; h < kTcN; ++h) mine |= x[h] > m[h] + kTcTauLog2;
+      const bool need = named_bar_or(1, 128, mine);
       bool raise = false;
       float alpha[kTcN];
 #pragma unroll
-      for (int h = 0; h < kTcN; ++h) {
-        const float mm = fmaxf(fmaxf(sh.red[b][0][h], sh.red[b][1][h]), fmaxf(sh.red[b][2][h], sh.red[b][3][h]));
-        alpha[h] = 1.0f;
-        if (u == 0) {
-          m[h] = mm == -INFINITY ? 0.0f : mm;  // padded heads (and no visible key) use 0
-        } else if (mm > m[h] + kTcTauLog2) {
-          alpha[h] = ex2_approx(m[h] - mm);
-          m[h] = mm;
-          raise = true;
+      for (int h = 0; h < kTcN; ++h) alpha[h] = 1.0f;
+      if (need) {
+        // the tile's maximum per head over its 128 keys: warp, then the four warps
+        float mt[kTcN];
+#pragma unroll
+        for (int h = 0; h < kTcN; ++h) {
+          mt[h] = x[h];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], off));
+        }
+        if (lane_id() == 0) {
+#pragma unroll
+          for (int h = 0; h < kTcN; ++h) sh.red[b][warp][h] = mt[h];
+        }
+        // (sh.red[b] is written again at a later tile, after every thread has
+        // passed the next tile's barrier, so after this tile's reads)
+        ok = named_bar_and(1, 128, ok);
+        if (!ok) break;
+#pragma unroll
+        for (int h = 0; h < kTcN; ++h) {
+          const float mm = fmaxf(fmaxf(sh.red[b][0][h], sh.red[b][1][h]), fmaxf(sh.red[b][2][h], sh.red[b][3][h]));
+          if (u == 0) {
+            m[h] = mm == -INFINITY ? 0.0f : mm;  // padded heads (and no visible key) use 0
+          } else if (mm > m[h] + kTcTauLog2) {
+            alpha[h] = ex2_approx(m[h] - mm);
+            m[h] = mm;
+            raise = true;
+          }
         }
       }
       // (the same values in every thread: `raise` is uniform)
