@@ -422,7 +422,9 @@ def _time_iters(fn, iters, flush=None, warmup=3):
     import torch
 
     stream = torch.cuda.current_stream()
-    for _ in range(warmup):
+    for _ in range(warmup):  # as the timed calls run, flush included
+        if flush is not None:
+            flush()
         fn()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
@@ -474,11 +476,22 @@ def side_measurements(peaks, peak_src, iters=8):
         ms_f = _time_iters(lambda: api.fa_fwd(q, k, v, causal, scale, o=o, lse=lse), iters, fl)
         ms_b = _time_iters(lambda: api.fa_bwd(q, k, v, o, lse, do, causal, scale, dq=dq, dk=dk, dv=dv,
                                               workspace=ws), iters, fl)
+
+        def step():
+            api.fa_fwd(q, k, v, causal, scale, o=o, lse=lse)
+            api.fa_bwd(q, k, v, o, lse, do, causal, scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+        ms_s = _time_iters(step, iters, fl)
         f, b = flops_step(B, H, N, d, causal)
+        # fwd_ms and bwd_ms time each call on its own (L2 flushed before each
+        # where the inputs fit in it); step_ms times the forward and backward
+        # back to back in one region, as the headline step is timed (L2
+        # flushed between steps only).
         out["cases"][name] = {
             "B": B, "H": H, "N": N, "d": d, "causal": causal, "l2_flush": fl is not None,
             "fwd_ms": ms_f, "bwd_ms": ms_b, "fwd_tflops": f / ms_f / 1e9, "bwd_tflops": b / ms_b / 1e9,
-            "fwdbwd_tflops": (f + b) / (ms_f + ms_b) / 1e9, "fwdbwd_frac": (f + b) / (ms_f + ms_b) / 1e9 / bf16_peak}
+            "fwdbwd_tflops": (f + b) / (ms_f + ms_b) / 1e9, "fwdbwd_frac": (f + b) / (ms_f + ms_b) / 1e9 / bf16_peak,
+            "step_ms": ms_s, "step_tflops": (f + b) / ms_s / 1e9, "step_frac": (f + b) / ms_s / 1e9 / bf16_peak}
 
     w = inputs.GPT2
     for causal in (True, False):
