@@ -54,6 +54,32 @@ def test_workspace_size(lib):
     assert lib.fa_bwd_workspace_size(0, 1, 1, 64) == 0
 
 
+def _grouped_decode_chunks(B, Hkv, N):
+    """Chunks per (batch, key/value head) of the grouped decode: one resident
+    wave of two CTAs per SM on 152 SMs while B*Hkv is below it, else the split
+    (1..4) with the fewest waves per unit of work; chunks whole 128-key tiles."""
+    wave, units, tiles = 2 * 152, B * Hkv, -(-N // 128)
+    if units < wave:
+        ns = wave // units
+    else:
+        ns = min(range(1, 5), key=lambda c: (-(-(units * c) // wave) / c, c))
+    ns = max(1, min(ns, tiles))
+    chunk = -(-(-(-N // ns)) // 128) * 128
+    return -(-N // chunk)
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,chunks", [
+    (1, 32, 8, 131072, 128, 38),   # 8 key/value heads: 304 CTAs, one wave
+    (8, 32, 8, 8192, 128, 4),      # 64 heads x 4 chunks of 2048 keys
+    (32, 64, 8, 4096, 128, 1),     # 256 heads: one chunk each
+    (32, 32, 16, 4096, 64, 4),     # 512 heads: 2048 CTAs in 7 waves beat 1 to 3 chunks
+    (2, 4, 2, 63, 64, 1),          # fewer keys than a tile
+])
+def test_grouped_decode_workspace_follows_the_chunk_plan(lib, B, H, Hkv, N, d, chunks):
+    assert _grouped_decode_chunks(B, Hkv, N) == chunks
+    assert lib.fa_decode_workspace_size(B, H, Hkv, N, d) == B * H * chunks * (d + 4) * 4
+
+
 ALIGNED = 0x10000
 
 
