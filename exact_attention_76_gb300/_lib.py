@@ -43,6 +43,7 @@ SIGNATURES = {
     "fa_measure_ex2_rate": ([_P, _P, _Z, _P], _I),
     "fa_debug_exp2_poly": ([_P, _P, _L, _I, _P], _I),
     "fa_decode_workspace_size": ([_I, _I, _I, _I, _I], _Z),
+    "fa_bwd_gqa_workspace_size": ([_I, _I, _I, _I, _I], _Z),
     "fa_decode": ([_P, _P, _P, _P, _P, _P, _Z, _I, _I, _I, _I, _I, _F, _P], _I),
 }
 

@@ -81,7 +81,7 @@ def fa_bwd_gqa(q, k, v, o, lse, dO, causal: bool, scale: float, dq=None, dk=None
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = fa_bwd_workspace_size(B, H, N, d)
+    need = fa_bwd_gqa_workspace_size(B, H, Hkv, N, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _lib.check("fa_bwd_gqa", lib.fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
@@ -132,6 +132,12 @@ def fa_bwd_window(q, k, v, o, lse, dO, window: int, scale: float, dq=None, dk=No
 
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(_lib.load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd_gqa_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
+    """Workspace bytes for fa_bwd_gqa (room for the dK and dV accumulators when
+    it would split a group's query heads over CTAs)."""
+    return int(_lib.load().fa_bwd_gqa_workspace_size(B, H, Hkv, N, d))
 
 
 def fa_bwd(q, k, v, o, lse, dO, causal: bool, scale: float, dq=None, dk=None, dv=None, workspace=None,

@@ -231,6 +231,31 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return round16(rows * sizeof(float)) + rows * d * sizeof(float);
 }
 
+namespace {
+
+// Grouped-query backward with one CTA per query head (partial dK and dV added
+// into fp32 accumulators) rather than per key/value head: when the key/value
+// heads give fewer than two waves of CTAs on 152 SMs (multi-query and small
+// groups of heads), where the per-key/value-head CTAs would walk every query
+// head of their group one after the other.
+bool bwd_split_heads(int B, int H, int Hkv, int N) {
+  if (Hkv <= 0 || H % Hkv != 0 || Hkv == H) return false;
+  const long long ctas = static_cast<long long>(B) * Hkv * ((N + 127) / 128);
+  return ctas < 2 * 152;
+}
+
+size_t kv_acc_bytes(int B, int Hkv, int N, int d) {
+  return round16(static_cast<size_t>(B) * Hkv * N * d * sizeof(float));
+}
+
+}  // namespace
+
+size_t fa_bwd_gqa_workspace_size(int B, int H, int Hkv, int N, int d) {
+  const size_t base = fa_bwd_workspace_size(B, H, N, d);
+  if (base == 0 || Hkv <= 0 || H % Hkv != 0) return 0;
+  return bwd_split_heads(B, H, Hkv, N) ? base + 2 * kv_acc_bytes(B, Hkv, N, d) : base;
+}
+
 fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, int B, int H, int N, int d,
                             void* stream) {
   fa_status st;
@@ -283,10 +308,24 @@ fa_status bwd_common(const void* q, const void* k, const void* v, const void* o,
   float* Dvec = static_cast<float*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + round16(rows * sizeof(float)));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // One CTA per query head when the workspace has room for the dK and dV
+  // accumulators (fa_bwd_gqa_workspace_size) and the heads call for it.
+  const size_t acc = kv_acc_bytes(B, Hkv, N, d);
+  const bool split = window == 0 && bwd_split_heads(B, H, Hkv, N) && workspace_bytes >= need + 2 * acc;
+  float* dk_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + need);
+  float* dv_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + need + acc);
+  if (split && cudaMemsetAsync(dk_acc, 0, 2 * acc, s) != cudaSuccess) return FA_ERR_LAUNCH;
   if ((st = launch_bwd_preprocess(o, dO, Dvec, dq_acc, static_cast<long long>(rows), d, s)) != FA_OK) return st;
-  BwdArgs a{q, k, v, lse, dO, Dvec, dq_acc, dk, dv, B, H, N, d, causal, scale, Hkv, window};
+  BwdArgs a{q, k, v, lse, dO, Dvec, dq_acc, split ? static_cast<void*>(dk_acc) : dk,
+            split ? static_cast<void*>(dv_acc) : dv, B, H, N, d, causal, scale, Hkv, window, split};
   if ((st = launch_bwd_main(a, s)) != FA_OK) return st;
-  return launch_bwd_dq_convert(dq_acc, dq, static_cast<long long>(rows), d, scale, s);
+  if ((st = launch_bwd_dq_convert(dq_acc, dq, static_cast<long long>(rows), d, scale, s)) != FA_OK) return st;
+  if (split) {
+    const long long kv_rows = static_cast<long long>(B) * Hkv * N;
+    if ((st = launch_bwd_dq_convert(dk_acc, dk, kv_rows, d, 1.0f, s)) != FA_OK) return st;
+    if ((st = launch_bwd_dq_convert(dv_acc, dv, kv_rows, d, 1.0f, s)) != FA_OK) return st;
+  }
+  return FA_OK;
 }
 
 }  // namespace

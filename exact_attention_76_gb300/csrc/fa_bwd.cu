@@ -238,8 +238,11 @@ __device__ __forceinline__ void bwd_item(int item, int BH, int n_blk, int group,
   bh = base_head + (r - kb * g_heads);
 }
 
-// WIN: causal sliding window of `window` keys.
-template <int D, bool WIN>
+// WIN: causal sliding window of `window` keys.  SPLIT (grouped-query heads):
+// one CTA per (query head, key block) instead of per (key/value head, key
+// block); each CTA adds its partial dK and dV (fp32) into accumulators of the
+// key/value head by TMA reduce-adds, so a group's query heads run in parallel.
+template <int D, bool WIN, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
@@ -264,17 +267,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_blk = (N + 127) / 128;
   // bh: the K/V head of this CTA (BH of them); its query heads are the
   // `qgroup` consecutive heads qh0 .. qh0 + qgroup - 1 (grouped-query
-  // attention; qgroup = 1 when every query head has its own K/V head).
-  int bh, kb;
-  bwd_item(static_cast<int>(blockIdx.x), BH, n_blk, head_group, bh, kb);
+  // attention; qgroup = 1 when every query head has its own K/V head).  With
+  // SPLIT the items are query heads (BH of them) and bh is derived: the CTA
+  // takes one query head, qh0, of the K/V head bh.
+  int item_h, kb;
+  bwd_item(static_cast<int>(blockIdx.x), BH, n_blk, head_group, item_h, kb);
   const int hkv = H / qgroup;
-  const int qh0 = (bh / hkv) * H + (bh % hkv) * qgroup;
+  const int bh = SPLIT ? (item_h / H) * hkv + (item_h % H) / qgroup : item_h;
+  const int qh0 = SPLIT ? item_h : (bh / hkv) * H + (bh % hkv) * qgroup;
+  const int heads = SPLIT ? 1 : qgroup;  // query heads this CTA walks
   const int i_begin = causal ? kb : 0;
   // With a sliding window of `window` keys (causal), the last query that sees
   // key kb*128 + 127 is kb*128 + 126 + window.
   const int i_end = WIN ? min(n_blk, (kb * 128 + 126 + window) / 128 + 1) : n_blk;
   const int n_per = i_end - i_begin;  // query blocks per query head
-  const int n_it = qgroup * n_per;
+  const int n_it = heads * n_per;
   // Every role walks the same (query head, query block) sequence: query
   // blocks i_begin .. i_end-1 of head qh0, then of qh0 + 1, and so on.
   struct QCursor {
@@ -698,7 +705,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (measured against per-thread row stores: +4 % on the backward at N = 512
     // and 1024, d = 128).  At d = 128 each warpgroup's 64 columns are a box of
     // their own; at d = 64 the two halves share one box.
-    {
+    if constexpr (SPLIT) {
+      // This CTA's part of dV (fp32), its 32-column blocks staged with the
+      // 128-byte swizzle (warpgroup 0 in K's dead space, 1 in Q's first
+      // stage) and added into the K/V head's accumulator by TMA reduce-adds.
+      constexpr int kCols = D / 2;
+      bool ok2 = ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd);
+      uint8_t* stage = smem + (half ? C::kOffQ : C::kOffK);
+      if (ok2) {
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < kCols; cc += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + C::kTmDV + half * kCols + cc, rr);
+          tmem_ld_wait(rr);
+          uint8_t* row = stage + (cc / 32) * C::kBlockBytes + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(row + ((static_cast<uint32_t>(c) ^ swz) << 4)) =
+                make_uint4(rr[4 * c], rr[4 * c + 1], rr[4 * c + 2], rr[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+      }
+      ok2 = named_bar_and(2 + half, 128, ok2);
+      if (ok2 && (warp & 3) == 0 && lane_id() == 0) {
+#pragma unroll
+        for (int cc = 0; cc < kCols; cc += 32)
+          tma_reduce_add_3d(&map_dv, half * kCols + cc, kb * 128, bh, stage + (cc / 32) * C::kBlockBytes);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+    } else {
       constexpr int kCols = D / 2;
       bool ok2 = ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd);
       if (ok2) {
@@ -808,8 +845,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (leader) bulk_wait_read_all();
     // dK = scale * sum_i dS_i^T Q_i, staged in V's dead space (D / 64 boxes of
-    // 64 columns) and written by TMA stores.
-    {
+    // 64 columns) and written by TMA stores; with SPLIT this CTA's part in
+    // fp32 (32-column blocks in V's dead space, then Q's second stage), added
+    // into the K/V head's accumulator by TMA reduce-adds.
+    if constexpr (SPLIT) {
+      constexpr int kInV = C::kTileBytes / C::kBlockBytes;  // blocks that fit in V's space
+      auto blk = [&](int b) { return smem + (b < kInV ? C::kOffV + b * C::kBlockBytes
+                                                       : C::kOffQ + C::kTileBytes + (b - kInV) * C::kBlockBytes); };
+      bool ok2 = ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd);
+      if (ok2) {
+        tc_fence_after();
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + lane_base + C::kTmDK + b * 32, rr);
+          tmem_ld_wait(rr);
+          uint8_t* row = blk(b) + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(row + ((static_cast<uint32_t>(c) ^ swz) << 4)) =
+                make_float4(__uint_as_float(rr[4 * c]) * scale, __uint_as_float(rr[4 * c + 1]) * scale,
+                            __uint_as_float(rr[4 * c + 2]) * scale, __uint_as_float(rr[4 * c + 3]) * scale);
+        }
+        fence_proxy_async_smem();
+      }
+      ok2 = named_bar_and(1, 128, ok2);
+      if (ok2 && leader) {
+#pragma unroll
+        for (int b = 0; b < D / 32; ++b) tma_reduce_add_3d(&map_dk, b * 32, kb * 128, bh, blk(b));
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+    } else {
       bool ok2 = ok && mbar_wait(&sh.acc_done, 0, &sh.abort, &g_err_bwd);
       if (ok2) {
         tc_fence_after();
@@ -849,19 +916,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool WIN>
+template <int D, bool WIN, bool SPLIT>
 fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
   const int BHq = a.B * a.H;     // query heads
-  const int BH = a.B * a.Hkv;    // key/value heads: one CTA column each
+  const int BH = a.B * a.Hkv;    // key/value heads: one CTA column each (SPLIT: one per query head)
   const int qgroup = a.H / a.Hkv;
   CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  // SPLIT: dk and dv are the fp32 accumulators, reduced into like dq_acc.
+  const int kv_eb = SPLIT ? 4 : 2, kv_box = SPLIT ? 32 : 64;
   if (!encode_rows_map(&mq, a.q, 2, D, a.N, BHq, 64, 128) || !encode_rows_map(&mk, a.k, 2, D, a.N, BH, 64, 128) ||
       !encode_rows_map(&mv, a.v, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdo, a.dO, 2, D, a.N, BHq, 64, 128) ||
       !encode_rows_map(&mdq, a.dq_acc, 4, D, a.N, BHq, 32, 128) ||
-      !encode_rows_map(&mdk, a.dk, 2, D, a.N, BH, 64, 128) || !encode_rows_map(&mdv, a.dv, 2, D, a.N, BH, 64, 128))
+      !encode_rows_map(&mdk, a.dk, kv_eb, D, a.N, BH, kv_box, 128) ||
+      !encode_rows_map(&mdv, a.dv, kv_eb, D, a.N, BH, kv_box, 128))
     return FA_ERR_LAUNCH;
-  auto kern = fa_bwd_main_kernel<D, WIN>;
+  auto kern = fa_bwd_main_kernel<D, WIN, SPLIT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
     return FA_ERR_LAUNCH;
   if (C::kRegSplit) {
@@ -874,12 +944,13 @@ fa_status launch_bwd_main_impl(const BwdArgs& a, cudaStream_t stream) {
   const int n_blk = (a.N + 127) / 128;
   // Heads per group: Q, dO (bf16) and the dQ accumulator (fp32) of a group
   // should stay within about 48 MB of the L2.
-  const long long head_bytes = static_cast<long long>(a.N) * D * (2 + 2 + 4) * qgroup;
+  const int items = SPLIT ? BHq : BH;
+  const long long head_bytes = static_cast<long long>(a.N) * D * (2 + 2 + 4) * (SPLIT ? 1 : qgroup);
   int group = static_cast<int>(std::max<long long>(1, (48ll << 20) / head_bytes));
-  group = std::min(group, BH);
-  dim3 grid(static_cast<unsigned>(n_blk * BH));
+  group = std::min(group, items);
+  dim3 grid(static_cast<unsigned>(n_blk * items));
   const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), C::kSmemBytes, stream, mq, mk, mv, mdo, mdq, mdk, mdv,
-                                   a.lse, a.D, BH, a.N, a.causal, a.scale, a.scale * kLog2e, group, a.H, qgroup,
+                                   a.lse, a.D, items, a.N, a.causal, a.scale, a.scale * kLog2e, group, a.H, qgroup,
                                    a.window);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -914,8 +985,11 @@ fa_status launch_bwd_preprocess(const void* o, const void* dO, float* D, float* 
 
 fa_status launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   if (a.window > 0)
-    return a.d == 64 ? launch_bwd_main_impl<64, true>(a, stream) : launch_bwd_main_impl<128, true>(a, stream);
-  return a.d == 64 ? launch_bwd_main_impl<64, false>(a, stream) : launch_bwd_main_impl<128, false>(a, stream);
+    return a.d == 64 ? launch_bwd_main_impl<64, true, false>(a, stream) : launch_bwd_main_impl<128, true, false>(a, stream);
+  if (a.split_heads)
+    return a.d == 64 ? launch_bwd_main_impl<64, false, true>(a, stream) : launch_bwd_main_impl<128, false, true>(a, stream);
+  return a.d == 64 ? launch_bwd_main_impl<64, false, false>(a, stream)
+                   : launch_bwd_main_impl<128, false, false>(a, stream);
 }
 
 fa_status launch_bwd_dq_convert(const float* dq_acc, void* dq, long long rows, int d, float scale,

@@ -73,6 +73,9 @@ struct BwdArgs {
   float scale;
   int Hkv;  // key/value heads of k, v, dk, dv; H % Hkv == 0
   int window = 0;  // causal sliding window of this many keys (0: none)
+  // dk and dv are fp32 accumulators (zeroed) into which one CTA per query
+  // head adds its part (grouped-query heads; not with a window)
+  bool split_heads = false;
 };
 
 fa_status launch_fwd_bf16(const FwdArgs& a, cudaStream_t stream);

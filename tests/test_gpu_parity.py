@@ -139,16 +139,27 @@ def test_gqa_forward_backward(H, Hkv, N, d, causal):
     scale = 1.0 / math.sqrt(d)
     qd, kd, vd, dod = to_dev(q, k, v, do)
     o, lse = api.fa_fwd_gqa(qd, kd, vd, causal, scale)
-    dq, dk, dv = api.fa_bwd_gqa(qd, kd, vd, o, lse, dod, causal, scale)
+    # With fa_bwd_gqa_workspace_size bytes these few key/value heads take the
+    # split path (one CTA per query head, dK and dV added into accumulators);
+    # with fa_bwd_workspace_size bytes the path that sums a group on chip.
+    full = api.fa_bwd_gqa_workspace_size(B, H, Hkv, N, d)
+    base = api.fa_bwd_workspace_size(B, H, N, d)
+    assert full > base
+    grads = {}
+    for tag, nbytes in (("split", full), ("group", base)):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        grads[tag] = api.fa_bwd_gqa(qd, kd, vd, o, lse, dod, causal, scale, workspace=ws)
     torch.cuda.synchronize()
     o_ref, l_ref = oracle.forward_gqa(q, k, v, causal, scale)
     assert max_abs(f64(o), o_ref) <= O_MAX_ABS
     assert max_abs(f64(lse), l_ref) <= L_MAX_ABS
     o_report(f64(o), o_ref, oracle.forward_gqa(q, k, v.abs(), causal, scale)[0], N,
              f"gqa H{H} Hkv{Hkv} N{N} d{d} c{int(causal)}")
-    for name, got, ref in zip(("dQ", "dK", "dV"), (dq, dk, dv), oracle.backward_gqa(q, k, v, do, causal, scale)):
-        e = rel_fro(f64(got), ref)
-        assert e <= GRAD_REL_FRO, f"{name} rel-Frobenius {e:.3e}"
+    refs = oracle.backward_gqa(q, k, v, do, causal, scale)
+    for tag, (dq, dk, dv) in grads.items():
+        for name, got, ref in zip(("dQ", "dK", "dV"), (dq, dk, dv), refs):
+            e = rel_fro(f64(got), ref)
+            assert e <= GRAD_REL_FRO, f"{tag} {name} rel-Frobenius {e:.3e}"
 
 
 # ---------------------------------------------------------------- more work items than SMs
