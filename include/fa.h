@@ -113,9 +113,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  *               head); with fa_bwd_gqa_workspace_size(B, H, Hkv, N, d) bytes
  *               the split described below may be used.
  * Each CTA owns one key/value head's block of keys and loops over all query
- * heads of its group, so dK and dV are summed on chip without atomics.  When
- * the key/value heads are too few to fill the GPU (multi-query attention,
- * small groups) and the workspace holds fa_bwd_gqa_workspace_size bytes, each
+ * heads of its group, so dK and dV are summed on chip without atomics.  For
+ * groups of four query heads or more, or key/value heads too few to fill the
+ * GPU, and when the workspace holds fa_bwd_gqa_workspace_size bytes, each
  * CTA takes one query head instead and adds its part of dK and dV into fp32
  * accumulators in the workspace by reduce-adds (their low bits may then vary
  * run to run, as dQ's do), converted to bf16 at the end.
@@ -128,8 +128,9 @@ fa_status fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
 /*
  * Workspace bytes for fa_bwd_gqa: fa_bwd_workspace_size(B, H, N, d), plus two
  * fp32 [B,Hkv,N,d] accumulators when fa_bwd_gqa would split the query heads of
- * a group over CTAs (fewer than two waves of per-key/value-head CTAs).  0 for
- * invalid shapes.  Host only; no GPU needed.
+ * a group over CTAs (groups of four query heads or more, or fewer than two
+ * waves of per-key/value-head CTAs).  0 for invalid shapes.  Host only; no GPU
+ * needed.
  */
 size_t fa_bwd_gqa_workspace_size(int B, int H, int Hkv, int N, int d);
 

@@ -81,12 +81,15 @@ def test_grouped_decode_workspace_follows_the_chunk_plan(lib, B, H, Hkv, N, d, c
 
 
 def test_gqa_workspace_size(lib):
-    # room for the fp32 dK and dV accumulators only when the key/value heads
-    # give fewer than two waves of per-key/value-head CTAs on 152 SMs
+    # room for the fp32 dK and dV accumulators only for groups of four query
+    # heads or more, or when the key/value heads give fewer than two waves of
+    # per-key/value-head CTAs on 152 SMs
     base = lib.fa_bwd_workspace_size(2, 32, 8192, 128)
     assert lib.fa_bwd_gqa_workspace_size(2, 32, 32, 8192, 128) == base          # every head its own
-    assert lib.fa_bwd_gqa_workspace_size(2, 32, 8, 8192, 128) == base           # 1024 CTAs
+    assert lib.fa_bwd_gqa_workspace_size(2, 32, 16, 8192, 128) == base          # groups of 2, 2048 CTAs
+    assert lib.fa_bwd_gqa_workspace_size(2, 32, 8, 8192, 128) == base + 2 * 2 * 8 * 8192 * 128 * 4  # groups of 4
     assert lib.fa_bwd_gqa_workspace_size(2, 32, 1, 8192, 128) == base + 2 * 2 * 1 * 8192 * 128 * 4  # 128 CTAs
+    assert lib.fa_bwd_gqa_workspace_size(1, 4, 2, 128, 64) == lib.fa_bwd_workspace_size(1, 4, 128, 64) + 2 * 2 * 128 * 64 * 4  # 2 CTAs
     assert lib.fa_bwd_gqa_workspace_size(2, 32, 3, 8192, 128) == 0             # 3 does not divide 32
     assert lib.fa_bwd_gqa_workspace_size(2, 4, 1, 1, 64) == lib.fa_bwd_workspace_size(2, 4, 1, 64) + 2 * 2 * 64 * 4
 
