@@ -8,13 +8,15 @@
 //   delta  = max |y| / 448     (one fp32 per tensor, 448 = largest e4m3)
 //   code   = e4m3_rne(y / delta)
 //
-// One warp per row of d values (d / 32 per lane).  The rotation is a fast
-// Walsh-Hadamard transform: butterflies (a, b) -> (a + b, a - b) over the
-// index bits, first the bits inside a lane's registers, then the lane bits
-// through warp shuffles.  Per tensor: three launches -- max |y| (atomic max on
-// the float's bit pattern, valid for non-negative floats), the codes, and
-// delta.  Per block (block quantisation of the same section: blocks of B_r x d
-// or B_c x d rows, one scale each): one launch, one CTA per block.
+// One warp per row of d values (d / 32 per lane, one vector load).  The
+// rotation is a fast Walsh-Hadamard transform: butterflies (a, b) -> (a + b,
+// a - b) over the index bits, first the bits inside a lane's registers, then
+// the lane bits through warp shuffles.  Per tensor: three launches -- max |y|
+// (atomic max on the float's bit pattern, valid for non-negative floats), the
+// codes, and delta; each warp keeps four rows' loads in flight.  Per block
+// (block quantisation of the same section: blocks of B_r x d or B_c x d rows,
+// one scale each): one launch, one CTA per block, which holds up to 128 rows
+// in registers so that the block is read once.
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
@@ -24,18 +26,39 @@ namespace fa {
 
 namespace {
 
+// This lane's d / 32 values of a row, in one vector load (x is 16-byte
+// aligned, so every lane's part is aligned to its size).
 template <int D, typename T>
-__device__ __forceinline__ void load_row_rotated(const T* __restrict__ x, long long row, bool rotate,
-                                                 float (&v)[D / 32]) {
+__device__ __forceinline__ void load_row(const T* __restrict__ x, long long row, float (&v)[D / 32]) {
+  constexpr int E = D / 32;
+  const T* src = x + row * D + static_cast<int>(lane_id()) * E;
+  if constexpr (sizeof(T) == 4) {
+    if constexpr (E == 4) {
+      const float4 t = __ldg(reinterpret_cast<const float4*>(src));
+      v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    } else {
+      const float2 t = __ldg(reinterpret_cast<const float2*>(src));
+      v[0] = t.x; v[1] = t.y;
+    }
+  } else {
+    if constexpr (E == 4) {
+      const uint2 t = __ldg(reinterpret_cast<const uint2*>(src));
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
+      v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+    } else {
+      const uint32_t t = __ldg(reinterpret_cast<const unsigned int*>(src));
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t));
+      v[0] = a.x; v[1] = a.y;
+    }
+  }
+}
+
+// y = x H / sqrt(d) of the row whose lane values are v.
+template <int D>
+__device__ __forceinline__ void rotate_row(float (&v)[D / 32]) {
   constexpr int E = D / 32;
   const int lane = static_cast<int>(lane_id());
-  const T* src = x + row * D + lane * E;
-#pragma unroll
-  for (int j = 0; j < E; ++j) {
-    if constexpr (sizeof(T) == 2) v[j] = __bfloat162float(src[j]);
-    else v[j] = static_cast<float>(src[j]);
-  }
-  if (!rotate) return;
   // index bits inside the lane: e = lane * E + j
 #pragma unroll
   for (int h = 1; h < E; h <<= 1) {
@@ -63,40 +86,78 @@ __device__ __forceinline__ void load_row_rotated(const T* __restrict__ x, long l
   for (int j = 0; j < E; ++j) v[j] *= norm;
 }
 
+// This lane's 4 e4m3 codes (or 2 at d = 64) of y / delta, stored at dst.
+template <int D>
+__device__ __forceinline__ void store_codes(uint8_t* dst, const float (&v)[D / 32], float delta) {
+  if constexpr (D / 32 == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta),
+                                                    __fdiv_rn(v[2], delta), __fdiv_rn(v[3], delta));
+  } else {
+    const uint32_t w = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta), 0.f, 0.f);
+    *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w & 0xffffu);
+  }
+}
+
+constexpr int kQRowsInFlight = 4;  // rows a warp loads before working on them
+
 template <int D, typename T>
 __global__ void __launch_bounds__(256) fp8q_amax_kernel(const T* __restrict__ x, long long rows, int rotate,
                                                         unsigned int* __restrict__ amax_bits) {
+  constexpr int E = D / 32, U = kQRowsInFlight;
   const long long warps = static_cast<long long>(gridDim.x) * 8;
   float m = 0.f;
-  for (long long row = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row < rows; row += warps) {
-    float v[D / 32];
-    load_row_rotated<D>(x, row, rotate != 0, v);
+  for (long long row0 = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row0 < rows; row0 += U * warps) {
+    float v[U][E];
 #pragma unroll
-    for (int j = 0; j < D / 32; ++j) m = fmaxf(m, fabsf(v[j]));
+    for (int u = 0; u < U; ++u) {
+      const long long row = row0 + u * warps;
+      if (row < rows) {
+        load_row<D>(x, row, v[u]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < E; ++j) v[u][j] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (rotate) rotate_row<D>(v[u]);
+#pragma unroll
+      for (int j = 0; j < E; ++j) m = fmaxf(m, fabsf(v[u][j]));
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (lane_id() == 0) atomicMax(amax_bits, __float_as_uint(m));
+  // the CTA's maximum first: one atomic per CTA on the shared word
+  __shared__ float s_part[8];
+  if (lane_id() == 0) s_part[warp_id()] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, s_part[i]);
+    atomicMax(amax_bits, __float_as_uint(m));
+  }
 }
 
 template <int D, typename T>
 __global__ void __launch_bounds__(256) fp8q_codes_kernel(const T* __restrict__ x, long long rows, int rotate,
                                                          const unsigned int* __restrict__ amax_bits,
                                                          uint8_t* __restrict__ codes) {
-  constexpr int E = D / 32;
+  constexpr int E = D / 32, U = kQRowsInFlight;
   const float amax = __uint_as_float(*amax_bits);
   const float delta = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   const long long warps = static_cast<long long>(gridDim.x) * 8;
-  for (long long row = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row < rows; row += warps) {
-    float v[E];
-    load_row_rotated<D>(x, row, rotate != 0, v);
-    uint8_t* dst = codes + row * D + lane_id() * E;
-    if constexpr (E == 4) {
-      *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta),
-                                                      __fdiv_rn(v[2], delta), __fdiv_rn(v[3], delta));
-    } else {
-      const uint32_t w = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta), 0.f, 0.f);
-      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w & 0xffffu);
+  for (long long row0 = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row0 < rows; row0 += U * warps) {
+    float v[U][E];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (row0 + u * warps < rows) load_row<D>(x, row0 + u * warps, v[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long row = row0 + u * warps;
+      if (row < rows) {
+        if (rotate) rotate_row<D>(v[u]);
+        store_codes<D>(codes + row * D + lane_id() * E, v[u], delta);
+      }
     }
   }
 }
@@ -124,44 +185,71 @@ fa_status launch_impl(const void* x, int rotate, void* codes, float* descale, lo
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-// Block storage: one CTA per (block of block_rows rows, sequence); each warp
-// takes every 8th row of the block, first for max |y|, then for the codes.
-template <int D, typename T>
-__global__ void __launch_bounds__(256) fp8qb_kernel(const T* __restrict__ x, int N, int block_rows, int rotate,
+// Block storage: one CTA per (block of block_rows rows, sequence).  With a
+// rotation or fp32 input, up to 128 rows a block are held in registers (warp w
+// takes rows w, w + 8, ..., all loaded before any is worked on) and read once;
+// otherwise (and for longer blocks) the block is read twice, for max |y| and
+// for the codes, the second time mostly from L1 (measured: bf16 without a
+// rotation ran 15 % slower held, at half the CTAs per SM).
+constexpr int kQbRowsPerWarp = 16;
+
+// (The held form at three CTAs per SM: measured faster than at the two its
+// unbounded register count allowed.)
+template <int D, typename T, bool HELD>
+__global__ void __launch_bounds__(256, HELD ? 3 : 1) fp8qb_kernel(const T* __restrict__ x, int N, int block_rows, int rotate,
                                                     uint8_t* __restrict__ codes, float* __restrict__ descale) {
-  constexpr int E = D / 32;
+  constexpr int E = D / 32, R = HELD ? kQbRowsPerWarp : 1;
   __shared__ float s_part[8];
   const int blk = static_cast<int>(blockIdx.x);
   const long long seq = blockIdx.y;
   const int r0 = blk * block_rows;
   const int r1 = min(N, r0 + block_rows);
   const long long base = seq * N;
+  const int w = static_cast<int>(warp_id());
+  float v[R][E];
   float m = 0.f;
-  for (int row = r0 + static_cast<int>(warp_id()); row < r1; row += 8) {
-    float v[E];
-    load_row_rotated<D>(x, base + row, rotate != 0, v);
+  if constexpr (HELD) {
 #pragma unroll
-    for (int j = 0; j < E; ++j) m = fmaxf(m, fabsf(v[j]));
+    for (int u = 0; u < R; ++u)
+      if (r0 + w + 8 * u < r1) load_row<D>(x, base + r0 + w + 8 * u, v[u]);
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      if (r0 + w + 8 * u < r1) {
+        if (rotate) rotate_row<D>(v[u]);
+#pragma unroll
+        for (int j = 0; j < E; ++j) m = fmaxf(m, fabsf(v[u][j]));
+      }
+    }
+  } else {
+    for (int row = r0 + w; row < r1; row += 8) {
+      float t[E];
+      load_row<D>(x, base + row, t);
+      if (rotate) rotate_row<D>(t);
+#pragma unroll
+      for (int j = 0; j < E; ++j) m = fmaxf(m, fabsf(t[j]));
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (lane_id() == 0) s_part[warp_id()] = m;
+  if (lane_id() == 0) s_part[w] = m;
   __syncthreads();
   float amax = s_part[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_part[w]);
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, s_part[i]);
   const float delta = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   if (threadIdx.x == 0) descale[seq * gridDim.x + blk] = delta;
-  for (int row = r0 + static_cast<int>(warp_id()); row < r1; row += 8) {
-    float v[E];
-    load_row_rotated<D>(x, base + row, rotate != 0, v);
-    uint8_t* dst = codes + (base + row) * D + lane_id() * E;
-    if constexpr (E == 4) {
-      *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta),
-                                                      __fdiv_rn(v[2], delta), __fdiv_rn(v[3], delta));
-    } else {
-      const uint32_t w = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta), 0.f, 0.f);
-      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w & 0xffffu);
+  if constexpr (HELD) {
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      const int row = r0 + w + 8 * u;
+      if (row < r1) store_codes<D>(codes + (base + row) * D + lane_id() * E, v[u], delta);
+    }
+  } else {
+    for (int row = r0 + w; row < r1; row += 8) {
+      float t[E];
+      load_row<D>(x, base + row, t);
+      if (rotate) rotate_row<D>(t);
+      store_codes<D>(codes + (base + row) * D + lane_id() * E, t, delta);
     }
   }
 }
@@ -170,8 +258,12 @@ template <int D, typename T>
 fa_status launch_blocks_impl(const void* x, int rotate, int block_rows, void* codes, float* descale, int seqs, int N,
                              cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>((N + block_rows - 1) / block_rows), static_cast<unsigned>(seqs));
-  fp8qb_kernel<D, T><<<grid, 256, 0, s>>>(static_cast<const T*>(x), N, block_rows, rotate,
-                                          static_cast<uint8_t*>(codes), descale);
+  if (block_rows <= 8 * kQbRowsPerWarp && (rotate || sizeof(T) == 4))
+    fp8qb_kernel<D, T, true><<<grid, 256, 0, s>>>(static_cast<const T*>(x), N, block_rows, rotate,
+                                                  static_cast<uint8_t*>(codes), descale);
+  else
+    fp8qb_kernel<D, T, false><<<grid, 256, 0, s>>>(static_cast<const T*>(x), N, block_rows, rotate,
+                                                   static_cast<uint8_t*>(codes), descale);
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
