@@ -131,6 +131,8 @@ def test_large_logits_rescale_path():
     (6, 2, 333, 64, False),    # ragged tail
     (8, 4, 512, 128, True),
     (4, 2, 130, 64, True),
+    (8, 2, 1, 128, True),      # one key: every block is the last, all but one row past the end
+    (8, 1, 17, 64, False),
 ])
 def test_gqa_forward_backward(H, Hkv, N, d, causal):
     B = 2
