@@ -86,14 +86,46 @@ __device__ __forceinline__ void rotate_row(float (&v)[D / 32]) {
   for (int j = 0; j < E; ++j) v[j] *= norm;
 }
 
+// y / delta as a product with a two-word reciprocal: inv_hi + inv_lo carries
+// 448 / max|y| to about 2^-48 relative (inv_hi = RN(448 / A); the residual
+// 448 - inv_hi A of a correctly rounded quotient is exact in one fma, and
+// inv_lo is that residual over A), and code = e4m3(fma(y, inv_hi, y inv_lo))
+// rounds y 448 / max|y| once.  A quotient that falls exactly on an e4m3
+// midpoint -- common with bf16 input, whose short significands make ratios
+// such as 21 = (25.5 / 448)^-1 x 1.1953125 exact -- stays exact and rounds to
+// even, as in the float64 definition; the single-word reciprocal or a quotient
+// by the rounded delta misses such a tie whenever their one rounding error
+// exceeds half an ulp of the quotient.  Both words are computed once per kernel
+// or block, so each code costs three operations instead of a division.
+// pre = 2^100 scales a maximum below 2^-100 up (exactly: |y| <= max|y|) so
+// that the reciprocal stays finite; an all-zero tensor or block has delta = 1
+// (pre = inv_hi = 1, inv_lo = 0), and an infinite maximum gives inv = 0.
+struct CodeScale {
+  float pre, hi, lo;
+};
+
+__device__ __forceinline__ CodeScale code_scale(float amax) {
+  if (!(amax > 0.f)) return {1.f, 1.f, 0.f};
+  const float pre = amax < 0x1p-100f ? 0x1p100f : 1.f;
+  const float a = amax * pre;
+  const float hi = __fdiv_rn(448.0f, a);
+  const float lo = a < INFINITY ? __fdiv_rn(__fmaf_rn(-hi, a, 448.0f), a) : 0.f;
+  return {pre, hi, lo};
+}
+
+__device__ __forceinline__ float code_value(float y, CodeScale c) {
+  const float s = y * c.pre;
+  return __fmaf_rn(s, c.hi, s * c.lo);
+}
+
 // This lane's 4 e4m3 codes (or 2 at d = 64) of y / delta, stored at dst.
 template <int D>
-__device__ __forceinline__ void store_codes(uint8_t* dst, const float (&v)[D / 32], float delta) {
+__device__ __forceinline__ void store_codes(uint8_t* dst, const float (&v)[D / 32], CodeScale c) {
   if constexpr (D / 32 == 4) {
-    *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta),
-                                                    __fdiv_rn(v[2], delta), __fdiv_rn(v[3], delta));
+    *reinterpret_cast<uint32_t*>(dst) = pack_e4m3x4(code_value(v[0], c), code_value(v[1], c),
+                                                    code_value(v[2], c), code_value(v[3], c));
   } else {
-    const uint32_t w = pack_e4m3x4(__fdiv_rn(v[0], delta), __fdiv_rn(v[1], delta), 0.f, 0.f);
+    const uint32_t w = pack_e4m3x4(code_value(v[0], c), code_value(v[1], c), 0.f, 0.f);
     *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w & 0xffffu);
   }
 }
@@ -143,8 +175,7 @@ __global__ void __launch_bounds__(256) fp8q_codes_kernel(const T* __restrict__ x
                                                          const unsigned int* __restrict__ amax_bits,
                                                          uint8_t* __restrict__ codes) {
   constexpr int E = D / 32, U = kQRowsInFlight;
-  const float amax = __uint_as_float(*amax_bits);
-  const float delta = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  const CodeScale cs = code_scale(__uint_as_float(*amax_bits));
   const long long warps = static_cast<long long>(gridDim.x) * 8;
   for (long long row0 = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row0 < rows; row0 += U * warps) {
     float v[U][E];
@@ -156,7 +187,7 @@ __global__ void __launch_bounds__(256) fp8q_codes_kernel(const T* __restrict__ x
       const long long row = row0 + u * warps;
       if (row < rows) {
         if (rotate) rotate_row<D>(v[u]);
-        store_codes<D>(codes + row * D + lane_id() * E, v[u], delta);
+        store_codes<D>(codes + row * D + lane_id() * E, v[u], cs);
       }
     }
   }
@@ -245,18 +276,18 @@ __device__ __forceinline__ void rotate_own_row(float (&v)[D]) {
 
 // A lane's row of codes (d bytes) from y / delta.
 template <int D>
-__device__ __forceinline__ void store_own_codes(uint8_t* __restrict__ dst, const float (&v)[D], float delta) {
+__device__ __forceinline__ void store_own_codes(uint8_t* __restrict__ dst, const float (&v)[D], CodeScale c) {
 #pragma unroll
   for (int k = 0; k < D; k += 16) {
     uint4 w;
-    w.x = pack_e4m3x4(__fdiv_rn(v[k], delta), __fdiv_rn(v[k + 1], delta), __fdiv_rn(v[k + 2], delta),
-                      __fdiv_rn(v[k + 3], delta));
-    w.y = pack_e4m3x4(__fdiv_rn(v[k + 4], delta), __fdiv_rn(v[k + 5], delta), __fdiv_rn(v[k + 6], delta),
-                      __fdiv_rn(v[k + 7], delta));
-    w.z = pack_e4m3x4(__fdiv_rn(v[k + 8], delta), __fdiv_rn(v[k + 9], delta), __fdiv_rn(v[k + 10], delta),
-                      __fdiv_rn(v[k + 11], delta));
-    w.w = pack_e4m3x4(__fdiv_rn(v[k + 12], delta), __fdiv_rn(v[k + 13], delta), __fdiv_rn(v[k + 14], delta),
-                      __fdiv_rn(v[k + 15], delta));
+    w.x = pack_e4m3x4(code_value(v[k], c), code_value(v[k + 1], c), code_value(v[k + 2], c),
+                      code_value(v[k + 3], c));
+    w.y = pack_e4m3x4(code_value(v[k + 4], c), code_value(v[k + 5], c), code_value(v[k + 6], c),
+                      code_value(v[k + 7], c));
+    w.z = pack_e4m3x4(code_value(v[k + 8], c), code_value(v[k + 9], c), code_value(v[k + 10], c),
+                      code_value(v[k + 11], c));
+    w.w = pack_e4m3x4(code_value(v[k + 12], c), code_value(v[k + 13], c), code_value(v[k + 14], c),
+                      code_value(v[k + 15], c));
     *reinterpret_cast<uint4*>(dst + k) = w;
   }
 }
@@ -296,8 +327,7 @@ __global__ void __launch_bounds__(kRotWarps * 32, 1) fp8q_codes_rot_kernel(const
                                                                           uint8_t* __restrict__ codes) {
   extern __shared__ float4 rot_smem[];
   uint8_t* buf = reinterpret_cast<uint8_t*>(rot_smem) + warp_id() * kRotWarpBytes<D, T>;
-  const float amax = __uint_as_float(*amax_bits);
-  const float delta = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  const CodeScale cs = code_scale(__uint_as_float(*amax_bits));
   const long long step = static_cast<long long>(gridDim.x) * kRotWarps * 32;
   for (long long row0 = (static_cast<long long>(blockIdx.x) * kRotWarps + warp_id()) * 32; row0 < rows;
        row0 += step) {
@@ -305,7 +335,7 @@ __global__ void __launch_bounds__(kRotWarps * 32, 1) fp8q_codes_rot_kernel(const
     rows_to_lanes<D>(x, row0, rows, buf, v);
     rotate_own_row<D>(v);
     const long long row = row0 + lane_id();
-    if (row < rows) store_own_codes<D>(codes + row * D, v, delta);
+    if (row < rows) store_own_codes<D>(codes + row * D, v, cs);
   }
 }
 
@@ -335,10 +365,9 @@ __global__ void __launch_bounds__(128) fp8qb_rot_kernel(const T* __restrict__ x,
   if (lane_id() == 0) s_part[w] = m;
   __syncthreads();
   const float amax = fmaxf(fmaxf(s_part[0], s_part[1]), fmaxf(s_part[2], s_part[3]));
-  const float delta = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-  if (threadIdx.x == 0) descale[seq * gridDim.x + blk] = delta;
+  if (threadIdx.x == 0) descale[seq * gridDim.x + blk] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   const long long row = row0 + lane_id();
-  if (row < r1) store_own_codes<D>(codes + (base + row) * D, v, delta);
+  if (row < r1) store_own_codes<D>(codes + (base + row) * D, v, code_scale(amax));
 }
 
 __global__ void fp8q_delta_kernel(float* __restrict__ descale) {
@@ -384,12 +413,13 @@ fa_status launch_impl(const void* x, int rotate, void* codes, float* descale, lo
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-// Block storage: one CTA per (block of block_rows rows, sequence).  With a
-// rotation or fp32 input, up to 128 rows a block are held in registers (warp w
-// takes rows w, w + 8, ..., all loaded before any is worked on) and read once;
-// otherwise (and for longer blocks) the block is read twice, for max |y| and
-// for the codes, the second time mostly from L1 (measured: bf16 without a
-// rotation ran 15 % slower held, at half the CTAs per SM).
+// Block storage: one CTA per (block of block_rows rows, sequence).  With fp32
+// input, up to 128 rows a block are held in registers (warp w takes rows w,
+// w + 8, ..., all loaded before any is worked on) and read once; otherwise
+// (bf16, and longer blocks) the block is read twice, for max |y| and for the
+// codes, the second time mostly from L1 (measured: bf16 without a rotation ran
+// 15 % slower held, at half the CTAs per SM).  Rotated blocks of up to 128
+// rows take the row-per-lane kernel above.
 constexpr int kQbRowsPerWarp = 16;
 
 // (The held form at three CTAs per SM: measured faster than at the two its
@@ -435,20 +465,20 @@ __global__ void __launch_bounds__(256, HELD ? 3 : 1) fp8qb_kernel(const T* __res
   float amax = s_part[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, s_part[i]);
-  const float delta = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-  if (threadIdx.x == 0) descale[seq * gridDim.x + blk] = delta;
+  if (threadIdx.x == 0) descale[seq * gridDim.x + blk] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  const CodeScale cs = code_scale(amax);
   if constexpr (HELD) {
 #pragma unroll
     for (int u = 0; u < R; ++u) {
       const int row = r0 + w + 8 * u;
-      if (row < r1) store_codes<D>(codes + (base + row) * D + lane_id() * E, v[u], delta);
+      if (row < r1) store_codes<D>(codes + (base + row) * D + lane_id() * E, v[u], cs);
     }
   } else {
     for (int row = r0 + w; row < r1; row += 8) {
       float t[E];
       load_row<D>(x, base + row, t);
       if (rotate) rotate_row<D>(t);
-      store_codes<D>(codes + (base + row) * D + lane_id() * E, t, delta);
+      store_codes<D>(codes + (base + row) * D + lane_id() * E, t, cs);
     }
   }
 }
@@ -464,12 +494,18 @@ fa_status launch_blocks_impl(const void* x, int rotate, int block_rows, void* co
       return FA_ERR_LAUNCH;
     fp8qb_rot_kernel<D, T><<<grid, 128, smem, s>>>(static_cast<const T*>(x), N, block_rows,
                                                   static_cast<uint8_t*>(codes), descale);
-  } else if (block_rows <= 8 * kQbRowsPerWarp && (rotate || sizeof(T) == 4))
-    fp8qb_kernel<D, T, true><<<grid, 256, 0, s>>>(static_cast<const T*>(x), N, block_rows, rotate,
-                                                  static_cast<uint8_t*>(codes), descale);
-  else
-    fp8qb_kernel<D, T, false><<<grid, 256, 0, s>>>(static_cast<const T*>(x), N, block_rows, rotate,
-                                                   static_cast<uint8_t*>(codes), descale);
+  } else {
+    bool held = false;
+    if constexpr (sizeof(T) == 4) {
+      held = block_rows <= 8 * kQbRowsPerWarp;
+      if (held)
+        fp8qb_kernel<D, T, true><<<grid, 256, 0, s>>>(static_cast<const T*>(x), N, block_rows, rotate,
+                                                      static_cast<uint8_t*>(codes), descale);
+    }
+    if (!held)
+      fp8qb_kernel<D, T, false><<<grid, 256, 0, s>>>(static_cast<const T*>(x), N, block_rows, rotate,
+                                                     static_cast<uint8_t*>(codes), descale);
+  }
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

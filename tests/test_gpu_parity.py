@@ -330,7 +330,7 @@ def _e4m3_codes(t):
 def _near_boundary_ok(got, ref_codes, x, y, t_scale, hadamard):
     """A code may differ from the fp64 reference only where y / delta lies
     within the kernel's fp32 error of an e4m3 rounding boundary: 2e-6 relative
-    (the division), plus, with the rotation, the rounding of the fp32 transform
+    (the scaling by 1 / delta), plus, with the rotation, the rounding of the fp32 transform
     -- log2(d) stages of additions whose partial sums are bounded by the row's
     l1 norm, then the 1/sqrt(d) scaling: (log2 d + 1) 2^-24 |x_row|_1 / sqrt(d)
     in y (t_scale converts y to y / delta)."""
@@ -404,6 +404,59 @@ def test_fp8_quantize_blocks_matches_reference(hadamard, d, block_rows, dtype):
     got = codes.cpu().numpy()
     inv = 1.0 / np.repeat(ref_deltas, block_rows, axis=-1)[..., :300, None]
     assert _near_boundary_ok(got, ref_codes, x, y, inv, hadamard).all()
+    assert (got == ref_codes).mean() > 0.999
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_quantize_bf16_codes_exact(d):
+    # bf16 input, no rotation: y / delta = 448 x / max|x| = 7 (a / b) 2^k with
+    # a, b the 8-bit significands.  Such a ratio is either short enough to be
+    # exact (an e4m3 value, or an e4m3 midpoint that rounds to even) or at
+    # least 2^-33 relative away from every fp32 rounding boundary, farther than
+    # the kernels' error (about 2^-47) and the float64 reference's, so every
+    # code equals the reference's.  0.6-1.0 % of these codes are exact
+    # midpoints; a quotient by the rounded fp32 delta turns 0.8 % of the codes
+    # of seed 16 at d = 128 the other way.
+    for seed in (7, 16):
+        x = inputs.draw_outlier_fp32(1, 2, 300, d, seed=seed)[0].to(torch.bfloat16)
+        y = f64(x)
+        codes, _ = api.fa_fp8_quantize(x.cuda(), False)
+        blocks, _ = api.fa_fp8_quantize_blocks(x.cuda(), False, 64)
+        torch.cuda.synchronize()
+        assert np.array_equal(codes.cpu().numpy(), oracle.quantize_e4m3_reference(y)[0])
+        assert np.array_equal(blocks.cpu().numpy(), oracle.quantize_e4m3_blocks_reference(y, 64)[0])
+
+
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_fp8_quantize_tiny_and_zero_scales(hadamard):
+    # max|y| below 2^-100 (the kernels scale y by 2^100 before the product with
+    # 448 / max|y|, which would overflow otherwise) and all-zero tensors and
+    # blocks (delta = 1, every code 0), per tensor and per 64-row block.
+    d = 128
+    x = inputs.draw_outlier_fp32(1, 2, 320, d, seed=9)[0]
+    y_of = (lambda t: oracle.rotate_rows(t)) if hadamard else f64
+    for t in (x * 2.0 ** -110, torch.zeros_like(x)):
+        codes, dsc = api.fa_fp8_quantize(t.cuda(), hadamard)
+        torch.cuda.synchronize()
+        y = y_of(t)
+        ref_codes, ref_delta = oracle.quantize_e4m3_reference(y)
+        assert abs(float(dsc.item()) - ref_delta) <= 1e-6 * ref_delta
+        got = codes.cpu().numpy()
+        assert _near_boundary_ok(got, ref_codes, t, y, 1.0 / ref_delta, hadamard).all()
+        assert (got == ref_codes).mean() > 0.999
+    f = torch.tensor([0.0, 2.0 ** -110, 1.0, 2.0 ** -60, 0.0])[torch.arange(320) // 64]
+    t = x * f[None, None, :, None] + 0.0  # +0 zero blocks: a rotated zero's sign follows the butterflies
+    codes, dsc = api.fa_fp8_quantize_blocks(t.cuda(), hadamard, 64)
+    torch.cuda.synchronize()
+    y = y_of(t)
+    ref_codes, ref_deltas = oracle.quantize_e4m3_blocks_reference(y, 64)
+    got_d = dsc.cpu().numpy().astype(np.float64).reshape(ref_deltas.shape)
+    np.testing.assert_allclose(got_d, ref_deltas, rtol=1e-6, atol=0)
+    assert np.all(got_d[..., [0, 4]] == 1.0)
+    got = codes.cpu().numpy()
+    assert np.all(got[..., :64, :] == 0) and np.all(got[..., 256:, :] == 0)
+    inv = 1.0 / np.repeat(ref_deltas, 64, axis=-1)[..., None]
+    assert _near_boundary_ok(got, ref_codes, t, y, inv, hadamard).all()
     assert (got == ref_codes).mean() > 0.999
 
 
