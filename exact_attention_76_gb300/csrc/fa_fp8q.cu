@@ -385,11 +385,11 @@ fa_status launch_impl(const void* x, int rotate, void* codes, float* descale, lo
   if (blocks < 1) blocks = 1;
   if (cudaMemsetAsync(descale, 0, sizeof(float), s) != cudaSuccess) return FA_ERR_LAUNCH;
   unsigned int* amax_bits = reinterpret_cast<unsigned int*>(descale);  // holds max |y| until the last step
-  if (rotate && sizeof(T) == 2) {
+  if (rotate) {
     // one row per lane: 32 rows a warp, one CTA of eight warps per SM
-    // (measured on a 1 x 16 x 16384 x 128 input: bf16 1.28 -> 1.39 TB/s; fp32
-    // input ran 2.02 -> 1.81, its codes pass at 212 registers and 8 warps per
-    // SM hiding less of the divisions, and keeps the lane-split form)
+    // (measured on a 1 x 16 x 16384 x 128 input against the lane-split form:
+    // with a division per code bf16 ran 1.39 TB/s against 1.28; with the
+    // two-word reciprocal fp32 runs 2.29 against 2.21)
     const int smem = kRotWarps * kRotWarpBytes<D, T>;
     if (cudaFuncSetAttribute(fp8q_amax_rot_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess ||
