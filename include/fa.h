@@ -182,7 +182,9 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float
  *   x       : rows x d input, fp32 (x_dtype = 0) or bf16 (x_dtype = 1), device.
  *   hadamard: 1 to rotate each row by H/sqrt(d) (H the Sylvester Hadamard
  *             matrix; use it for Q and K, never for V), 0 to quantise as is.
- *   codes   : rows x d e4m3 codes out (1 byte each), device.
+ *   codes   : rows x d e4m3 codes out (1 byte each), device: e4m3_rne of
+ *             y * 448 / max|y| (y as is if all zero), the product rounded
+ *             once to fp32 and saturated at +-448.
  *   descale : one fp32 out, device: delta = max|y| / 448 (1 if all zero), so
  *             that y ~= delta * code.
  *   d in {64, 128}; rows >= 1.  Three launches on `stream`; the descale word
@@ -245,7 +247,8 @@ fa_status fa_fwd_fp8_blocks(const void* q8, const void* k8, const void* v8, cons
  *   block_rows : rows per block, 1..1024 (FA_FP8_BLOCK_Q for Q,
  *                FA_FP8_BLOCK_KV for K and V); the last block of a sequence
  *                holds the remaining N mod block_rows rows, if any.
- *   codes      : [seqs, N, d] e4m3 codes out, device.
+ *   codes      : [seqs, N, d] e4m3 codes out, device (rounded as in
+ *                fa_fp8_quantize, with each block's own max|y|).
  *   descale    : [seqs, ceil(N / block_rows)] fp32 out, device: per block
  *                delta = max|y| / 448 (1 if the block is all zero).
  *   d in {64, 128}; seqs in 1..65535; N >= 1.  One launch on `stream`.
