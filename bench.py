@@ -609,6 +609,49 @@ def run_fp8(args):
     return 0
 
 
+def run_quant(args):
+    """The FP8 quantisers on the FP8 workload's tensor shape (a side
+    measurement, not the bench's workload): B=1, H=16, N=16384, d=128, the
+    outlier draws of Q as fp32 and as bf16 input, per tensor and per 128-row
+    block, each with and without the Hadamard rotation.  Bytes per call: the
+    input read once and the e4m3 codes written (the per-tensor form reads its
+    input twice, for max|y| and for the codes, so its ceiling lies below the
+    copy figure).  A 256 MiB write flushes L2 between calls; each call is
+    timed with CUDA events on the launching stream."""
+    import torch
+
+    from exact_attention_76_gb300 import api, inputs
+    from exact_attention_76_gb300 import build as _build
+
+    _build.build()
+    B, H, N, d, block_rows = 1, 16, 16384, 128, 128
+    x32 = inputs.draw_outlier_fp32(B, H, N, d, seed=4)[0].cuda()
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    peaks, src = measured_peaks()
+    cases = {}
+    for x in (x32, x32.to(torch.bfloat16)):
+        codes = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+        desc = torch.empty(1, dtype=torch.float32, device="cuda")
+        desc_b = torch.empty(B * H, N // block_rows, dtype=torch.float32, device="cuda")
+        nbytes = x.numel() * (x.element_size() + 1)
+        for rot in (False, True):
+            for form, fn in (("tensor", lambda: api.fa_fp8_quantize(x, rot, codes=codes, descale=desc,
+                                                                    stream=stream)),
+                             ("blocks128", lambda: api.fa_fp8_quantize_blocks(x, rot, block_rows, codes=codes,
+                                                                              descale=desc_b, stream=stream))):
+                ms = _time_iters(fn, args.steps, flush=scratch.zero_, warmup=max(args.warmup, 3))
+                gbs = nbytes / ms / 1e6
+                name = f"{form}_{'fp32' if x.dtype == torch.float32 else 'bf16'}{'_rot' if rot else ''}"
+                cases[name] = {"ms": ms, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
+    best = max(c["GB/s"] for c in cases.values())
+    print(json.dumps({"metric": "fp8 quantiser throughput (input read once + codes written)", "value": best,
+                      "unit": "GB/s", "steps": args.steps, "higher_is_better": True, "dtype": "f32",
+                      "data": "synthetic", "config": {"workload": f"fp8q_B{B}_H{H}_N{N}_d{d}", "l2": "flushed"},
+                      "cases": cases, "peak": peaks["hbm_gbs"], "peak_source": src}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -623,7 +666,11 @@ def main():
     ap.add_argument("--mufu", action="store_true", help="measure the special-function unit's exp2 rate")
     ap.add_argument("--fp8", choices=["full", "causal"], default="",
                     help="time the FP8 forward on B=1 H=16 N=16384 d=128 instead (side measurement)")
+    ap.add_argument("--quant", action="store_true",
+                    help="time the FP8 quantisers on the FP8 workload's tensor shape instead (side measurement)")
     args = ap.parse_args()
+    if args.quant:
+        return run_quant(args)
     if args.decode:
         return run_decode(args)
     if args.fp8:

@@ -118,6 +118,16 @@ __device__ __forceinline__ float code_value(float y, CodeScale c) {
   return __fmaf_rn(s, c.hi, s * c.lo);
 }
 
+// The per-tensor codes kernels are launched while the max|y| kernel before
+// them finishes (programmatic dependent launch).  Their input x is only read
+// (by both kernels), so a CTA loads its first rows first and waits for the
+// maximum only when it needs the scale; the maximum itself is read after the
+// wait with a plain (not read-only-cached) load.
+__device__ __forceinline__ CodeScale scale_after_max_kernel(const unsigned int* amax_bits) {
+  pdl_wait_prior();
+  return code_scale(__uint_as_float(*reinterpret_cast<const volatile unsigned int*>(amax_bits)));
+}
+
 // This lane's 4 e4m3 codes (or 2 at d = 64) of y / delta, stored at dst.
 template <int D>
 __device__ __forceinline__ void store_codes(uint8_t* dst, const float (&v)[D / 32], CodeScale c) {
@@ -136,6 +146,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(256) fp8q_amax_kernel(const T* __restrict__ x, long long rows, int rotate,
                                                         unsigned int* __restrict__ amax_bits) {
   constexpr int E = D / 32, U = kQRowsInFlight;
+  pdl_launch_dependents();
   const long long warps = static_cast<long long>(gridDim.x) * 8;
   float m = 0.f;
   for (long long row0 = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row0 < rows; row0 += U * warps) {
@@ -172,16 +183,22 @@ __global__ void __launch_bounds__(256) fp8q_amax_kernel(const T* __restrict__ x,
 
 template <int D, typename T>
 __global__ void __launch_bounds__(256) fp8q_codes_kernel(const T* __restrict__ x, long long rows, int rotate,
-                                                         const unsigned int* __restrict__ amax_bits,
+                                                         const unsigned int* amax_bits,
                                                          uint8_t* __restrict__ codes) {
   constexpr int E = D / 32, U = kQRowsInFlight;
-  const CodeScale cs = code_scale(__uint_as_float(*amax_bits));
+  pdl_launch_dependents();
+  CodeScale cs{};
+  bool have_scale = false;
   const long long warps = static_cast<long long>(gridDim.x) * 8;
   for (long long row0 = static_cast<long long>(blockIdx.x) * 8 + warp_id(); row0 < rows; row0 += U * warps) {
     float v[U][E];
 #pragma unroll
     for (int u = 0; u < U; ++u)
       if (row0 + u * warps < rows) load_row<D>(x, row0 + u * warps, v[u]);
+    if (!have_scale) {
+      cs = scale_after_max_kernel(amax_bits);
+      have_scale = true;
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const long long row = row0 + u * warps;
@@ -298,6 +315,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(kRotWarps * 32, 1) fp8q_amax_rot_kernel(const T* __restrict__ x, long long rows,
                                                                          unsigned int* __restrict__ amax_bits) {
   extern __shared__ float4 rot_smem[];
+  pdl_launch_dependents();
   uint8_t* buf = reinterpret_cast<uint8_t*>(rot_smem) + warp_id() * kRotWarpBytes<D, T>;
   const long long step = static_cast<long long>(gridDim.x) * kRotWarps * 32;
   float m = 0.f;
@@ -323,17 +341,23 @@ __global__ void __launch_bounds__(kRotWarps * 32, 1) fp8q_amax_rot_kernel(const 
 
 template <int D, typename T>
 __global__ void __launch_bounds__(kRotWarps * 32, 1) fp8q_codes_rot_kernel(const T* __restrict__ x, long long rows,
-                                                                          const unsigned int* __restrict__ amax_bits,
+                                                                          const unsigned int* amax_bits,
                                                                           uint8_t* __restrict__ codes) {
   extern __shared__ float4 rot_smem[];
+  pdl_launch_dependents();
   uint8_t* buf = reinterpret_cast<uint8_t*>(rot_smem) + warp_id() * kRotWarpBytes<D, T>;
-  const CodeScale cs = code_scale(__uint_as_float(*amax_bits));
+  CodeScale cs{};
+  bool have_scale = false;
   const long long step = static_cast<long long>(gridDim.x) * kRotWarps * 32;
   for (long long row0 = (static_cast<long long>(blockIdx.x) * kRotWarps + warp_id()) * 32; row0 < rows;
        row0 += step) {
     float v[D];
     rows_to_lanes<D>(x, row0, rows, buf, v);
     rotate_own_row<D>(v);
+    if (!have_scale) {
+      cs = scale_after_max_kernel(amax_bits);
+      have_scale = true;
+    }
     const long long row = row0 + lane_id();
     if (row < rows) store_own_codes<D>(codes + row * D, v, cs);
   }
@@ -371,6 +395,7 @@ __global__ void __launch_bounds__(128) fp8qb_rot_kernel(const T* __restrict__ x,
 }
 
 __global__ void fp8q_delta_kernel(float* __restrict__ descale) {
+  pdl_wait_prior();
   const float amax = __uint_as_float(*reinterpret_cast<const unsigned int*>(descale));
   *descale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
 }
@@ -400,16 +425,20 @@ fa_status launch_impl(const void* x, int rotate, void* codes, float* descale, lo
     if (rblocks > sms) rblocks = sms;
     fp8q_amax_rot_kernel<D, T><<<static_cast<unsigned>(rblocks), kRotWarps * 32, smem, s>>>(
         static_cast<const T*>(x), rows, amax_bits);
-    fp8q_codes_rot_kernel<D, T><<<static_cast<unsigned>(rblocks), kRotWarps * 32, smem, s>>>(
-        static_cast<const T*>(x), rows, amax_bits, static_cast<uint8_t*>(codes));
-    fp8q_delta_kernel<<<1, 1, 0, s>>>(descale);
+    if (launch_pdl(fp8q_codes_rot_kernel<D, T>, dim3(static_cast<unsigned>(rblocks)), dim3(kRotWarps * 32), smem,
+                   s, static_cast<const T*>(x), rows, static_cast<const unsigned int*>(amax_bits),
+                   static_cast<uint8_t*>(codes)) != cudaSuccess ||
+        launch_pdl(fp8q_delta_kernel, dim3(1), dim3(1), 0, s, descale) != cudaSuccess)
+      return FA_ERR_LAUNCH;
     return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
   }
   fp8q_amax_kernel<D, T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const T*>(x), rows, rotate,
                                                                         amax_bits);
-  fp8q_codes_kernel<D, T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const T*>(x), rows, rotate,
-                                                                         amax_bits, static_cast<uint8_t*>(codes));
-  fp8q_delta_kernel<<<1, 1, 0, s>>>(descale);
+  if (launch_pdl(fp8q_codes_kernel<D, T>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                 static_cast<const T*>(x), rows, rotate, static_cast<const unsigned int*>(amax_bits),
+                 static_cast<uint8_t*>(codes)) != cudaSuccess ||
+      launch_pdl(fp8q_delta_kernel, dim3(1), dim3(1), 0, s, descale) != cudaSuccess)
+    return FA_ERR_LAUNCH;
   return cudaPeekAtLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -407,6 +407,25 @@ def test_fp8_quantize_blocks_matches_reference(hadamard, d, block_rows, dtype):
     assert (got == ref_codes).mean() > 0.999
 
 
+def test_fp8_quantize_back_to_back_calls():
+    # Calls queued back to back on one stream: each call's codes kernel starts
+    # while its max|y| kernel finishes and reads x before waiting for it, so a
+    # missing wait or a stale maximum (another call's) would show here.
+    xs = [(inputs.draw_outlier_fp32(1, 2, 300 + 37 * i, 128, seed=20 + i)[0] * 4.0 ** i).to(dt)
+          for i, dt in enumerate((torch.float32, torch.bfloat16, torch.float32))]
+    dev = [x.cuda() for x in xs]
+    torch.cuda.synchronize()
+    outs = [(x, had, api.fa_fp8_quantize(xd, had)) for x, xd in zip(xs, dev) for had in (False, True)]
+    torch.cuda.synchronize()
+    for x, had, (codes, dsc) in outs:
+        y = oracle.rotate_rows(x) if had else f64(x)
+        ref_codes, ref_delta = oracle.quantize_e4m3_reference(y)
+        assert abs(float(dsc.item()) - ref_delta) <= 1e-6 * ref_delta
+        got = codes.cpu().numpy()
+        assert _near_boundary_ok(got, ref_codes, x, y, 1.0 / ref_delta, had).all()
+        assert (got == ref_codes).mean() > 0.999
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_fp8_quantize_bf16_codes_exact(d):
     # bf16 input, no rotation: y / delta = 448 x / max|x| = 7 (a / b) 2^k with
