@@ -230,13 +230,14 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc, boo
                "r"(valid ? 16 : 0)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// Starts the copies of rows [row0, row0 + 32) (zeros past row_end) into the
+// warp's staging buffer, as one committed group.
 template <int D, typename T>
-__device__ __forceinline__ void rows_to_lanes(const T* __restrict__ x, long long row0, long long row_end,
-                                              uint8_t* __restrict__ wbuf, float (&v)[D]) {
+__device__ __forceinline__ void stage_rows(const T* __restrict__ x, long long row0, long long row_end,
+                                           uint8_t* __restrict__ wbuf) {
   constexpr int VEC = 16 / static_cast<int>(sizeof(T));  // elements per 16-byte copy
   constexpr int STRIDE = kRotRowElems<D, T>;
   constexpr int CHUNKS = 32 * D / VEC;
@@ -250,9 +251,18 @@ __device__ __forceinline__ void rows_to_lanes(const T* __restrict__ x, long long
     const bool valid = e < avail;
     cp_async16(tb + (e / D) * STRIDE + (e % D), valid ? src + e : src, valid);
   }
+  cp_async_commit();
+}
+
+// Waits for the staged rows and moves this lane's row into v; the buffer is
+// free for the next stage_rows when this returns.
+template <int D, typename T>
+__device__ __forceinline__ void take_row(const uint8_t* __restrict__ wbuf, float (&v)[D]) {
+  constexpr int VEC = 16 / static_cast<int>(sizeof(T));
+  constexpr int STRIDE = kRotRowElems<D, T>;
   cp_async_wait_all();
   __syncwarp();
-  const T* mine = tb + lane * STRIDE;
+  const T* mine = reinterpret_cast<const T*>(wbuf) + static_cast<int>(lane_id()) * STRIDE;
 #pragma unroll
   for (int k = 0; k < D; k += VEC) {
     const uint4 t = *reinterpret_cast<const uint4*>(mine + k);
@@ -270,6 +280,13 @@ __device__ __forceinline__ void rows_to_lanes(const T* __restrict__ x, long long
     }
   }
   __syncwarp();
+}
+
+template <int D, typename T>
+__device__ __forceinline__ void rows_to_lanes(const T* __restrict__ x, long long row0, long long row_end,
+                                              uint8_t* __restrict__ wbuf, float (&v)[D]) {
+  stage_rows<D, T>(x, row0, row_end, wbuf);
+  take_row<D, T>(wbuf, v);
 }
 
 // y = x H / sqrt(d) of a whole row held by one lane.
@@ -319,10 +336,12 @@ __global__ void __launch_bounds__(kRotWarps * 32, 1) fp8q_amax_rot_kernel(const 
   uint8_t* buf = reinterpret_cast<uint8_t*>(rot_smem) + warp_id() * kRotWarpBytes<D, T>;
   const long long step = static_cast<long long>(gridDim.x) * kRotWarps * 32;
   float m = 0.f;
-  for (long long row0 = (static_cast<long long>(blockIdx.x) * kRotWarps + warp_id()) * 32; row0 < rows;
-       row0 += step) {
+  long long row0 = (static_cast<long long>(blockIdx.x) * kRotWarps + warp_id()) * 32;
+  if (row0 < rows) stage_rows<D>(x, row0, rows, buf);
+  for (; row0 < rows; row0 += step) {
     float v[D];
-    rows_to_lanes<D>(x, row0, rows, buf, v);
+    take_row<D, T>(buf, v);
+    if (row0 + step < rows) stage_rows<D>(x, row0 + step, rows, buf);  // in flight during the butterflies
     rotate_own_row<D>(v);
 #pragma unroll
     for (int k = 0; k < D; ++k) m = fmaxf(m, fabsf(v[k]));
@@ -349,10 +368,12 @@ __global__ void __launch_bounds__(kRotWarps * 32, 1) fp8q_codes_rot_kernel(const
   CodeScale cs{};
   bool have_scale = false;
   const long long step = static_cast<long long>(gridDim.x) * kRotWarps * 32;
-  for (long long row0 = (static_cast<long long>(blockIdx.x) * kRotWarps + warp_id()) * 32; row0 < rows;
-       row0 += step) {
+  long long row0 = (static_cast<long long>(blockIdx.x) * kRotWarps + warp_id()) * 32;
+  if (row0 < rows) stage_rows<D>(x, row0, rows, buf);
+  for (; row0 < rows; row0 += step) {
     float v[D];
-    rows_to_lanes<D>(x, row0, rows, buf, v);
+    take_row<D, T>(buf, v);
+    if (row0 + step < rows) stage_rows<D>(x, row0 + step, rows, buf);
     rotate_own_row<D>(v);
     if (!have_scale) {
       cs = scale_after_max_kernel(amax_bits);
