@@ -384,8 +384,10 @@ __global__ void __launch_bounds__(kRotWarps * 32, 1) fp8q_codes_rot_kernel(const
   }
 }
 
-// Block storage with the rotation, blocks of at most 128 rows: one CTA of four
-// warps per block, each lane one row, the block read once.
+// Block storage with the rotation, blocks of at most 128 rows: one CTA per
+// block with a warp per 32 of its rows (so 64-row blocks run two warps, not
+// four of which two would rotate zeros), each lane one row, the block read
+// once.
 template <int D, typename T>
 __global__ void __launch_bounds__(128) fp8qb_rot_kernel(const T* __restrict__ x, int N, int block_rows,
                                                         uint8_t* __restrict__ codes, float* __restrict__ descale) {
@@ -409,7 +411,8 @@ __global__ void __launch_bounds__(128) fp8qb_rot_kernel(const T* __restrict__ x,
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   if (lane_id() == 0) s_part[w] = m;
   __syncthreads();
-  const float amax = fmaxf(fmaxf(s_part[0], s_part[1]), fmaxf(s_part[2], s_part[3]));
+  float amax = s_part[0];
+  for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) amax = fmaxf(amax, s_part[i]);
   if (threadIdx.x == 0) descale[seq * gridDim.x + blk] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
   const long long row = row0 + lane_id();
   if (row < r1) store_own_codes<D>(codes + (base + row) * D, v, code_scale(amax));
@@ -562,8 +565,9 @@ fa_status launch_blocks_impl(const void* x, int rotate, int block_rows, void* co
     if (cudaFuncSetAttribute(fp8qb_rot_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return FA_ERR_LAUNCH;
-    fp8qb_rot_kernel<D, T><<<grid, 128, smem, s>>>(static_cast<const T*>(x), N, block_rows,
-                                                  static_cast<uint8_t*>(codes), descale);
+    const int warps = (block_rows + 31) / 32;
+    fp8qb_rot_kernel<D, T><<<grid, 32 * warps, warps * kRotWarpBytes<D, T>, s>>>(
+        static_cast<const T*>(x), N, block_rows, static_cast<uint8_t*>(codes), descale);
   } else {
     bool held = false;
     if constexpr (sizeof(T) == 4) {
