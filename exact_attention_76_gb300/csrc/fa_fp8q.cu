@@ -8,15 +8,22 @@
 //   delta  = max |y| / 448     (one fp32 per tensor, 448 = largest e4m3)
 //   code   = e4m3_rne(y / delta)
 //
-// One warp per row of d values (d / 32 per lane, one vector load).  The
-// rotation is a fast Walsh-Hadamard transform: butterflies (a, b) -> (a + b,
-// a - b) over the index bits, first the bits inside a lane's registers, then
-// the lane bits through warp shuffles.  Per tensor: three launches -- max |y|
-// (atomic max on the float's bit pattern, valid for non-negative floats), the
-// codes, and delta; each warp keeps four rows' loads in flight.  Per block
-// (block quantisation of the same section: blocks of B_r x d or B_c x d rows,
-// one scale each): one launch, one CTA per block, which holds up to 128 rows
-// in registers so that the block is read once.
+// Two layouts of the work:
+//  * lane-split (no rotation, and rotated blocks of more than 128 rows): one
+//    warp per row of d values (d / 32 per lane, one vector load, several rows
+//    in flight); the rotation there is a fast Walsh-Hadamard transform whose
+//    butterflies (a, b) -> (a + b, a - b) run over the index bits, first those
+//    inside a lane's registers, then the lane bits through warp shuffles;
+//  * row per lane (every other rotated input): a warp stages 32 rows in
+//    shared memory and each lane transforms a whole row in registers, the
+//    same butterflies in the same order.
+// Per tensor: three launches -- max |y| (atomic max on the float's bit
+// pattern, valid for non-negative floats), the codes, and delta, the last two
+// launched while the one before finishes.  Per block (block quantisation of
+// the same section: blocks of B_r x d or B_c x d rows, one scale each): one
+// launch, one CTA per block; fp32 blocks of up to 128 rows are held in
+// registers, other unrotated blocks read twice (the second time from L1).
+// Every code is y * 448 / max|y| rounded once to fp32 (code_scale below).
 #include <cuda_bf16.h>
 
 #include "fa_common.cuh"
