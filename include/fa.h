@@ -24,6 +24,14 @@
  *    and a device error word per kernel family.
  *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy
  *    default stream.  Launches are asynchronous on that stream.
+ *  - CUDA graphs: the compute entry points only enqueue asynchronous work on
+ *    `stream` (kernels, some launched with programmatic stream serialization,
+ *    and memsets), so a call can be captured into a graph and replayed; the
+ *    captured launches keep that call's pointers, sizes and scale.  Make the
+ *    first call of each entry point outside a capture (it sets kernel
+ *    attributes and loads modules).  fa_device_error, fa_measure_ex2_rate and
+ *    the first fa_bwd_noalloc call on a device synchronise and cannot be
+ *    captured.
  *  - Supported shapes: B, H, N >= 1, d in {64, 128}; B * H <= 2^31 / N.
  *    Rows past N in the last tile of a head are handled inside the kernels
  *    (loads past the end read zeros; masked keys get weight 0; nothing is
