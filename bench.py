@@ -565,10 +565,13 @@ def run_decode(args):
 def run_fp8(args):
     """FP8 e4m3 forward on the FP8 workload (a side measurement, not the bench's
     workload): B=1, H=16, N=16384, d=128, Q, K, V drawn N(0,1) with 0.1 % of the
-    entries scaled by 10, stored as per-tensor e4m3 by the library's quantiser
-    with Q and K Hadamard-rotated first (the configuration that passes the FP8
-    error gate); timed with CUDA events on the launching stream against the
-    fp8 peak (the measured bf16 figure times 2, the nominal fp8:bf16 ratio)."""
+    entries scaled by 10, stored as e4m3 by the library's quantiser with Q and
+    K Hadamard-rotated first (the configuration that passes the FP8 error
+    gate): one scale per tensor, or with --fp8-blocks one per 128 rows of Q
+    and per 64 rows of K and V.  The codes (100 MB) fit in L2, so a 256 MiB
+    write flushes it between calls; each call is timed with CUDA events on the
+    launching stream, against the fp8 peak (the measured bf16 figure times 2,
+    the nominal fp8:bf16 ratio)."""
     import torch
 
     from exact_attention_76_gb300 import api, inputs
@@ -578,31 +581,32 @@ def run_fp8(args):
     causal = args.fp8 == "causal"
     B, H, N, d = 1, 16, 16384, 128
     q, k, v = (t.cuda() for t in inputs.draw_outlier_fp32(B, H, N, d, seed=4))
-    (q8, dq), (k8, dk), (v8, dv) = (api.fa_fp8_quantize(q, True), api.fa_fp8_quantize(k, True),
-                                    api.fa_fp8_quantize(v, False))
+    if args.fp8_blocks:
+        (q8, dq), (k8, dk), (v8, dv) = (api.fa_fp8_quantize_blocks(q, True, api.FP8_BLOCK_Q),
+                                        api.fa_fp8_quantize_blocks(k, True, api.FP8_BLOCK_KV),
+                                        api.fa_fp8_quantize_blocks(v, False, api.FP8_BLOCK_KV))
+        fwd, scales = api.fa_fwd_fp8_blocks, "block scales (128 rows of Q, 64 of K and V)"
+    else:
+        (q8, dq), (k8, dk), (v8, dv) = (api.fa_fp8_quantize(q, True), api.fa_fp8_quantize(k, True),
+                                        api.fa_fp8_quantize(v, False))
+        fwd, scales = api.fa_fwd_fp8, "per-tensor scales"
     del q, k, v
     o = torch.empty(B, H, N, d, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
     scale = 1.0 / math.sqrt(d)
     stream = torch.cuda.current_stream()
-    for _ in range(max(args.warmup, 3)):
-        api.fa_fwd_fp8(q8, k8, v8, dq, dk, dv, causal, scale, o=o, lse=lse, stream=stream)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        api.fa_fwd_fp8(q8, k8, v8, dq, dk, dv, causal, scale, o=o, lse=lse, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ms = _time_iters(lambda: fwd(q8, k8, v8, dq, dk, dv, causal, scale, o=o, lse=lse, stream=stream), args.steps,
+                     flush=scratch.zero_, warmup=max(args.warmup, 3))
     fl, _ = flops_step(B, H, N, d, causal)
     tflops = fl / ms / 1e9
     peaks, src = measured_peaks()
     peak = 2.0 * peaks["bf16_tflops"]
-    print(json.dumps({"metric": "attention fwd TFLOPS (fp8 e4m3, per-tensor scales, d=128, 1xGB300)",
+    tag = f"fp8_B{B}_H{H}_N{N}_d{d}_{args.fp8}" + ("_blocks" if args.fp8_blocks else "")
+    print(json.dumps({"metric": f"attention fwd TFLOPS (fp8 e4m3, {scales}, d=128, 1xGB300)",
                       "value": tflops, "unit": "TFLOP/s", "steps": args.steps, "ms_per_step": ms,
                       "higher_is_better": True, "dtype": "e4m3", "data": "synthetic",
-                      "config": {"workload": f"fp8_B{B}_H{H}_N{N}_d{d}_{args.fp8}"},
+                      "config": {"workload": tag, "l2": "flushed"},
                       "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                                    "frac": tflops / peak, "peak_source": src + " bf16 burst x 2 (fp8:bf16)"}}),
           flush=True)
@@ -666,6 +670,7 @@ def main():
     ap.add_argument("--mufu", action="store_true", help="measure the special-function unit's exp2 rate")
     ap.add_argument("--fp8", choices=["full", "causal"], default="",
                     help="time the FP8 forward on B=1 H=16 N=16384 d=128 instead (side measurement)")
+    ap.add_argument("--fp8-blocks", action="store_true", help="with --fp8: block-scaled codes and fa_fwd_fp8_blocks")
     ap.add_argument("--quant", action="store_true",
                     help="time the FP8 quantisers on the FP8 workload's tensor shape instead (side measurement)")
     args = ap.parse_args()
