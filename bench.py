@@ -656,6 +656,77 @@ def run_quant(args):
     return 0
 
 
+def run_variant(args):
+    """Grouped-query or sliding-window attention, forward + backward (a side
+    measurement, not the bench's workload): --gqa B,H,Hkv,N,d (causal) or
+    --window B,H,N,d,W.  Inputs are seeded N(0,1) draws made on the device;
+    the forward, the backward and the two back to back are each timed with
+    CUDA events on the launching stream, and a 256 MiB write flushes L2
+    between calls when the inputs fit in it.  FLOPs: grouped-query attention
+    counts as H full heads under the causal convention; the window counts its
+    visible pairs only (row i sees min(i + 1, W) keys), backward 2.5 x
+    forward."""
+    import torch
+
+    from exact_attention_76_gb300 import api
+    from exact_attention_76_gb300 import build as _build
+
+    _build.build()
+    if args.gqa:
+        B, H, Hkv, N, d = (int(x) for x in args.gqa.split(","))
+        W = 0
+    else:
+        B, H, N, d, W = (int(x) for x in args.window.split(","))
+        Hkv = H
+    g = torch.Generator(device="cuda").manual_seed(1)
+    q, do = (torch.randn(B, H, N, d, device="cuda", generator=g).to(torch.bfloat16) for _ in range(2))
+    k, v = (torch.randn(B, Hkv, N, d, device="cuda", generator=g).to(torch.bfloat16) for _ in range(2))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = torch.empty_like(q), torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if W:
+        ws = torch.empty(api.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+
+        def fwd():
+            api.fa_fwd_window(q, k, v, W, scale, o=o, lse=lse)
+
+        def bwd():
+            api.fa_bwd_window(q, k, v, o, lse, do, W, scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+        pairs = N * W - W * (W - 1) // 2 if N >= W else N * (N + 1) // 2
+        f = 4.0 * B * H * d * pairs
+        name = f"window{W}_B{B}_H{H}_N{N}_d{d}"
+    else:
+        ws = torch.empty(api.fa_bwd_gqa_workspace_size(B, H, Hkv, N, d), dtype=torch.uint8, device="cuda")
+
+        def fwd():
+            api.fa_fwd_gqa(q, k, v, True, scale, o=o, lse=lse)
+
+        def bwd():
+            api.fa_bwd_gqa(q, k, v, o, lse, do, True, scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+        f, _ = flops_step(B, H, N, d, True)
+        name = f"gqa_B{B}_H{H}_Hkv{Hkv}_N{N}_d{d}_c"
+    b = 2.5 * f
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    in_bytes = (2 * B * H + 2 * B * Hkv) * N * d * 2
+    fl = scratch.zero_ if in_bytes <= L2_BYTES else None
+    warm = max(args.warmup, 3)
+    ms_f = _time_iters(fwd, args.steps, fl, warm)
+    ms_b = _time_iters(bwd, args.steps, fl, warm)
+    ms_s = _time_iters(lambda: (fwd(), bwd()), args.steps, fl, warm)
+    peaks, src = measured_peaks()
+    step_tflops = (f + b) / ms_s / 1e9
+    print(json.dumps({"metric": "attention fwd+bwd TFLOPS (bf16)", "value": step_tflops, "unit": "TFLOP/s",
+                      "steps": args.steps, "ms_per_step": ms_s, "higher_is_better": True, "dtype": "bf16",
+                      "data": "synthetic", "config": {"workload": name, "l2": "flushed" if fl else "inputs > L2"},
+                      "fwd_ms": ms_f, "bwd_ms": ms_b, "fwd_tflops": f / ms_f / 1e9, "bwd_tflops": b / ms_b / 1e9,
+                      "roofline": {"bound": "tensor", "achieved": step_tflops, "peak": peaks["bf16_tflops"],
+                                   "unit": "TFLOP/s", "frac": step_tflops / peaks["bf16_tflops"],
+                                   "peak_source": src + " bf16 burst"}}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -671,11 +742,15 @@ def main():
     ap.add_argument("--fp8", choices=["full", "causal"], default="",
                     help="time the FP8 forward on B=1 H=16 N=16384 d=128 instead (side measurement)")
     ap.add_argument("--fp8-blocks", action="store_true", help="with --fp8: block-scaled codes and fa_fwd_fp8_blocks")
+    ap.add_argument("--gqa", default="", help="B,H,Hkv,N,d: time grouped-query fwd+bwd instead (side measurement)")
+    ap.add_argument("--window", default="", help="B,H,N,d,W: time sliding-window fwd+bwd instead (side measurement)")
     ap.add_argument("--quant", action="store_true",
                     help="time the FP8 quantisers on the FP8 workload's tensor shape instead (side measurement)")
     args = ap.parse_args()
     if args.quant:
         return run_quant(args)
+    if args.gqa or args.window:
+        return run_variant(args)
     if args.decode:
         return run_decode(args)
     if args.fp8:
