@@ -568,10 +568,11 @@ def run_fp8(args):
     entries scaled by 10, stored as e4m3 by the library's quantiser with Q and
     K Hadamard-rotated first (the configuration that passes the FP8 error
     gate): one scale per tensor, or with --fp8-blocks one per 128 rows of Q
-    and per 64 rows of K and V.  The codes (100 MB) fit in L2, so a 256 MiB
-    write flushes it between calls; each call is timed with CUDA events on the
-    launching stream, against the fp8 peak (the measured bf16 figure times 2,
-    the nominal fp8:bf16 ratio)."""
+    and per 64 rows of K and V.  --fp8-shape B,H,N,d replaces the shape.  The
+    default shape's codes (100 MB) fit in L2, so a 256 MiB write flushes it
+    between calls; each call is timed with CUDA events on the launching
+    stream, against the fp8 peak (the measured bf16 figure times 2, the
+    nominal fp8:bf16 ratio)."""
     import torch
 
     from exact_attention_76_gb300 import api, inputs
@@ -579,7 +580,7 @@ def run_fp8(args):
 
     _build.build()
     causal = args.fp8 == "causal"
-    B, H, N, d = 1, 16, 16384, 128
+    B, H, N, d = (int(x) for x in args.fp8_shape.split(","))
     q, k, v = (t.cuda() for t in inputs.draw_outlier_fp32(B, H, N, d, seed=4))
     if args.fp8_blocks:
         (q8, dq), (k8, dk), (v8, dv) = (api.fa_fp8_quantize_blocks(q, True, api.FP8_BLOCK_Q),
@@ -603,7 +604,7 @@ def run_fp8(args):
     peaks, src = measured_peaks()
     peak = 2.0 * peaks["bf16_tflops"]
     tag = f"fp8_B{B}_H{H}_N{N}_d{d}_{args.fp8}" + ("_blocks" if args.fp8_blocks else "")
-    print(json.dumps({"metric": f"attention fwd TFLOPS (fp8 e4m3, {scales}, d=128, 1xGB300)",
+    print(json.dumps({"metric": f"attention fwd TFLOPS (fp8 e4m3, {scales}, d={d}, 1xGB300)",
                       "value": tflops, "unit": "TFLOP/s", "steps": args.steps, "ms_per_step": ms,
                       "higher_is_better": True, "dtype": "e4m3", "data": "synthetic",
                       "config": {"workload": tag, "l2": "flushed"},
@@ -742,6 +743,7 @@ def main():
     ap.add_argument("--fp8", choices=["full", "causal"], default="",
                     help="time the FP8 forward on B=1 H=16 N=16384 d=128 instead (side measurement)")
     ap.add_argument("--fp8-blocks", action="store_true", help="with --fp8: block-scaled codes and fa_fwd_fp8_blocks")
+    ap.add_argument("--fp8-shape", default="1,16,16384,128", help="with --fp8: B,H,N,d")
     ap.add_argument("--gqa", default="", help="B,H,Hkv,N,d: time grouped-query fwd+bwd instead (side measurement)")
     ap.add_argument("--window", default="", help="B,H,N,d,W: time sliding-window fwd+bwd instead (side measurement)")
     ap.add_argument("--quant", action="store_true",
