@@ -148,11 +148,16 @@ __device__ __forceinline__ void store_codes(uint8_t* dst, const float (&v)[D / 3
 }
 
 constexpr int kQRowsInFlight = 4;  // rows a warp loads before working on them
+// The per-tensor kernels keep twice as many fp32 rows in flight (measured on
+// 1 x 16 x 16384 x 128, L2 flushed: fp32 59.9 -> 56.9 us a call; bf16 ran
+// 41.9 -> 45.7 with eight and keeps four).
+template <typename T>
+constexpr int kTensorRowsInFlight = sizeof(T) == 4 ? 2 * kQRowsInFlight : kQRowsInFlight;
 
 template <int D, typename T>
 __global__ void __launch_bounds__(256) fp8q_amax_kernel(const T* __restrict__ x, long long rows, int rotate,
                                                         unsigned int* __restrict__ amax_bits) {
-  constexpr int E = D / 32, U = kQRowsInFlight;
+  constexpr int E = D / 32, U = kTensorRowsInFlight<T>;
   pdl_launch_dependents();
   const long long warps = static_cast<long long>(gridDim.x) * 8;
   float m = 0.f;
@@ -192,7 +197,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(256) fp8q_codes_kernel(const T* __restrict__ x, long long rows, int rotate,
                                                          const unsigned int* amax_bits,
                                                          uint8_t* __restrict__ codes) {
-  constexpr int E = D / 32, U = kQRowsInFlight;
+  constexpr int E = D / 32, U = kTensorRowsInFlight<T>;
   pdl_launch_dependents();
   CodeScale cs{};
   bool have_scale = false;
