@@ -45,6 +45,12 @@ def flops_step(B, H, N, d, causal):
     return fwd, 2.5 * fwd
 
 
+def window_pairs(N, W):
+    """(query, key) pairs a sliding window of W keys leaves visible over N
+    rows: row i sees keys i - W + 1 .. i that exist, min(i + 1, W) of them."""
+    return N * W - W * (W - 1) // 2 if N >= W else N * (N + 1) // 2
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -694,8 +700,7 @@ def run_variant(args):
         def bwd():
             api.fa_bwd_window(q, k, v, o, lse, do, W, scale, dq=dq, dk=dk, dv=dv, workspace=ws)
 
-        pairs = N * W - W * (W - 1) // 2 if N >= W else N * (N + 1) // 2
-        f = 4.0 * B * H * d * pairs
+        f = 4.0 * B * H * d * window_pairs(N, W)
         name = f"window{W}_B{B}_H{H}_N{N}_d{d}"
     else:
         ws = torch.empty(api.fa_bwd_gqa_workspace_size(B, H, Hkv, N, d), dtype=torch.uint8, device="cuda")

@@ -78,3 +78,15 @@ def test_reference_arm_line_on_rank_zero(monkeypatch):
     line = json.loads(buf.getvalue())
     assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_window_pair_count_against_the_mask():
+    # The sliding-window side measurement counts FLOPs over the visible pairs;
+    # the count must equal the number of (i, j) with i - W < j <= i.
+    sys.path.insert(0, ROOT)
+    import bench
+
+    for N in (1, 5, 64, 130):
+        for W in (1, 3, 64, 129, 200):
+            brute = sum(1 for i in range(N) for j in range(N) if i - W < j <= i)
+            assert bench.window_pairs(N, W) == brute, (N, W)
