@@ -407,6 +407,25 @@ def test_fp8_quantize_blocks_matches_reference(hadamard, d, block_rows, dtype):
     assert (got == ref_codes).mean() > 0.999
 
 
+@pytest.mark.parametrize("block_rows,dtype", [(64, torch.float32), (128, torch.bfloat16)])
+def test_fp8_quantize_blocks_many_blocks(block_rows, dtype):
+    # Enough rotated blocks (1024 or 512 over 8 sequences) that every CTA of
+    # the block kernel takes several, staging the next one's rows while it
+    # transforms the current one; blocks differ in magnitude by up to 2^8.
+    x = inputs.draw_outlier_fp32(1, 8, 8192, 128, seed=13)[0]
+    x = (x * torch.exp2((torch.arange(8192) // 64 % 9).to(torch.float32) - 4.0)[None, None, :, None]).to(dtype)
+    codes, dsc = api.fa_fp8_quantize_blocks(x.cuda(), True, block_rows)
+    torch.cuda.synchronize()
+    y = oracle.rotate_rows(x)
+    ref_codes, ref_deltas = oracle.quantize_e4m3_blocks_reference(y, block_rows)
+    got_d = dsc.cpu().numpy().astype(np.float64).reshape(ref_deltas.shape)
+    np.testing.assert_allclose(got_d, ref_deltas, rtol=1e-6, atol=0)
+    got = codes.cpu().numpy()
+    inv = 1.0 / np.repeat(ref_deltas, block_rows, axis=-1)[..., None]
+    assert _near_boundary_ok(got, ref_codes, x, y, inv, True).all()
+    assert (got == ref_codes).mean() > 0.999
+
+
 def test_fp8_quantize_back_to_back_calls():
     # Calls queued back to back on one stream: each call's codes kernel starts
     # while its max|y| kernel finishes and reads x before waiting for it, so a
