@@ -387,12 +387,13 @@ def test_fp8_forward_with_incoherent_processing(causal, N, d):
 @pytest.mark.parametrize("hadamard", [False, True])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("block_rows,dtype", [(64, torch.float32), (128, torch.float32), (128, torch.bfloat16),
-                                              (48, torch.bfloat16), (48, torch.float32), (200, torch.float32)])
+                                              (48, torch.bfloat16), (48, torch.float32), (200, torch.float32),
+                                              (200, torch.bfloat16)])
 def test_fp8_quantize_blocks_matches_reference(hadamard, d, block_rows, dtype):
     # Same decision rule as the per-tensor quantiser: codes may differ only where
     # y/delta lies within the kernel's fp32 error of an e4m3 rounding boundary.
     # Blocks of 48 rows end inside a warp's 32 rows; 200 rows take the two-pass
-    # form.
+    # form (four rows in flight per warp), for both input types.
     x = inputs.draw_outlier_fp32(1, 3, 300, d, seed=8)[0]
     x = (x * torch.exp2(torch.arange(300, dtype=torch.float32) // 50 - 3.0)[None, None, :, None]).to(dtype)
     codes, dsc = api.fa_fp8_quantize_blocks(x.cuda(), hadamard, block_rows)
