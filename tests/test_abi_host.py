@@ -135,6 +135,46 @@ def test_fp8_argument_errors_before_any_launch(lib):
     assert lib.fa_fwd_fp8(p, p, p + 1, p, p, p, p, p, 1, 1, 128, 128, 0, 0.1, None) == 3
 
 
+def test_quantiser_argument_errors_before_any_launch(lib):
+    p = ALIGNED
+    q = lib.fa_fp8_quantize  # (x, x_dtype, hadamard, codes, descale, rows, d, stream)
+    assert q(None, 0, 0, p, p, 128, 128, None) == 1
+    assert q(p, 0, 0, p, None, 128, 128, None) == 1
+    assert q(p, 2, 0, p, p, 128, 128, None) == 1            # x_dtype
+    assert q(p, 0, 2, p, p, 128, 128, None) == 1            # hadamard flag
+    assert q(p, 0, 0, p, p, 0, 128, None) == 1              # rows
+    assert q(p, 0, 0, p, p, (1 << 31) + 1, 128, None) == 1
+    assert q(p, 0, 0, p, p, 128, 96, None) == 2             # d
+    assert q(p + 8, 0, 0, p, p, 128, 128, None) == 3        # misaligned x
+
+    def blk(x=p, dt=0, had=0, br=64, codes=p, desc=p, seqs=2, N=300, d=128):
+        return lib.fa_fp8_quantize_blocks(x, dt, had, br, codes, desc, seqs, N, d, None)
+
+    assert blk(br=0) == 1 and blk(br=1025) == 1
+    assert blk(seqs=0) == 1 and blk(seqs=65536) == 1
+    assert blk(N=0) == 1 and blk(dt=3) == 1 and blk(had=-1) == 1
+    assert blk(codes=None) == 1
+    assert blk(d=256) == 2
+    assert blk(desc=p + 4) == 3
+
+
+def test_decode_argument_errors_before_any_launch(lib):
+    p = ALIGNED
+
+    def dec(q=p, k=p, v=p, o=p, lse=p, ws=p, wsb=1 << 30, B=1, H=4, Hkv=2, N=100, d=128, scale=0.1):
+        return lib.fa_decode(q, k, v, o, lse, ws, wsb, B, H, Hkv, N, d, scale, None)
+
+    assert dec(q=None) == 1 and dec(lse=None) == 1
+    assert dec(B=0) == 1 and dec(N=0) == 1
+    assert dec(H=4, Hkv=3) == 1                             # Hkv must divide H
+    assert dec(H=34, Hkv=2) == 1                            # groups of at most 16 query heads
+    assert dec(d=96) == 2
+    assert dec(scale=0.0) == 1 and dec(scale=float("inf")) == 1
+    assert dec(ws=None) == 6 and dec(wsb=16) == 6           # workspace missing or too small
+    assert dec(ws=p + 8) == 3
+    assert dec(v=p + 4) == 3
+
+
 def test_measurement_and_exp2_hooks_reject_bad_arguments(lib):
     p = ALIGNED
     assert lib.fa_measure_ex2_rate(None, p, 1 << 20, None) == 1
