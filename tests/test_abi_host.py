@@ -175,6 +175,30 @@ def test_decode_argument_errors_before_any_launch(lib):
     assert dec(v=p + 4) == 3
 
 
+def test_gqa_and_window_argument_errors_before_any_launch(lib):
+    p = ALIGNED
+
+    def fg(Hkv=2, causal=1, d=128):
+        return lib.fa_fwd_gqa(p, p, p, p, p, 1, 4, Hkv, 128, d, causal, 0.1, None)
+
+    def bg(Hkv=2, causal=1, ws=p, wsb=1 << 30):
+        return lib.fa_bwd_gqa(p, p, p, p, p, p, p, p, p, ws, wsb, 1, 4, Hkv, 128, 128, causal, 0.1, None)
+
+    def fw(window=16, Hkv=2):
+        return lib.fa_fwd_window(p, p, p, p, p, 1, 4, Hkv, 128, 128, window, 0.1, None)
+
+    def bw(window=16, Hkv=2, ws=p, wsb=1 << 30):
+        return lib.fa_bwd_window(p, p, p, p, p, p, p, p, p, ws, wsb, 1, 4, Hkv, 128, 128, window, 0.1, None)
+
+    assert fg(Hkv=3) == 1 and fg(Hkv=0) == 1 and fg(causal=2) == 1   # Hkv must divide H
+    assert fg(d=80) == 2
+    assert bg(Hkv=3) == 1 and bg(causal=5) == 1
+    assert bg(ws=None) == 6 and bg(wsb=16) == 6 and bg(ws=p + 8) == 3
+    assert fw(window=0) == 1 and fw(window=-5) == 1 and fw(Hkv=3) == 1
+    assert bw(window=0) == 1 and bw(Hkv=3) == 1
+    assert bw(ws=None) == 6 and bw(wsb=16) == 6 and bw(ws=p + 8) == 3
+
+
 def test_measurement_and_exp2_hooks_reject_bad_arguments(lib):
     p = ALIGNED
     assert lib.fa_measure_ex2_rate(None, p, 1 << 20, None) == 1
